@@ -1,0 +1,534 @@
+#!/usr/bin/env python3
+"""Benchmark: direct conv2d forward (and the fused stencil) on one or more GPUs.
+
+Workload of the headline line: the 3-layer upscaling-style net on one
+1280x720 single-channel fp32 image (conv 5x5 1->32 + ReLU, conv 3x3 32->32
++ ReLU, conv 3x3 32->4), NHWC, synthetic seeded data and He-normal weights.
+A step is one forward pass of the three layers; `value` is conv GFLOP/s
+(2*N*H*W*Cin*Cout*R*S per layer), device-timed with CUDA events per step,
+with L2 flushed between steps (a 256 MiB write outside the timed events).
+The line also carries Mpixel/s, a per-workload breakdown of all five
+workloads, the roofline of the dominant kernel, the oracle's CPU timing,
+an end-to-end number through host buffers, SM clocks during the timed
+region and the number of kernel launches.
+
+--impl reference times the fp64 CPU oracle on the machine's host cores on a
+strip of the same workload (the same metric and unit).
+Multi-GPU: one independent replica per rank (the path has no exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "conv GFLOP/s and output Mpixel/s per config; % of FP32/HBM roofline"
+WORKLOAD = "3-layer upscaling net, 1x1280x720 fp32 (5x5 1->32 ReLU, 3x3 32->32 ReLU, 3x3 32->4)"
+L2_FLUSH_BYTES = 256 << 20
+FP32_LANES_PER_SM = 128          # FP32 FMA lanes per Blackwell SM (4 schedulers x 32)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the five-workload breakdown")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except OSError:
+        return None
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_key: str, src_hash: str):
+    """DRAM bytes per launch recorded from an ncu capture under profiles/, or
+    None when absent or taken on different kernel sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    try:
+        for line in open(path):
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel_key:
+                if parts[1] == src_hash:
+                    return float(parts[2])
+    except OSError:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax.append(float(p[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# The GPU arm
+# --------------------------------------------------------------------------
+
+
+def conv_flops(n, h, w, L):
+    return 2 * n * h * w * L.cin * L.cout * L.r * L.s
+
+
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    import synthetic as S
+    import stencil_conv2d_fwd_gb300 as sc
+
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    sc.load()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    stream = torch.cuda.current_stream()
+    props = torch.cuda.get_device_properties(dev)
+    n_sm = props.multi_processor_count
+    peaks = measured_peaks() or {}
+    sm_max_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    fp32_peak_tflops = n_sm * FP32_LANES_PER_SM * 2 * sm_max_mhz * 1e6 / 1e12
+    hbm_gbs = float(peaks.get("hbm_gbs", 6800.0))
+    hbm_src = "measured" if "hbm_gbs" in peaks else "fallback"
+
+    wl = S.config(3)
+    N, H, W = wl.n, wl.h, wl.w
+    layers = wl.layers
+    flops_layer = [conv_flops(N, H, W, L) for L in layers]
+    flops_step = sum(flops_layer)
+
+    xd = torch.from_numpy(wl.x).to(dev)  # Cin = 1: NCHW == NHWC
+    wds = [torch.from_numpy(L.w).to(dev) for L in layers]
+    bds = [torch.from_numpy(L.b).to(dev) for L in layers]
+    acts = [torch.empty(N * H * W * L.cout, device=dev) for L in layers]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev)
+
+    def step(ev=None):
+        src = xd
+        for li, L in enumerate(layers):
+            if ev is not None:
+                ev[li][0].record(stream)
+            rc = sc.conv2d_fwd(src, wds[li], bds[li], acts[li], N, H, W, L.cin, L.cout, L.r, L.s,
+                               sc.SC_NHWC, L.act, stream)
+            if rc != 0:
+                raise RuntimeError(f"conv2d_fwd layer {li + 1}: {sc.sc_status_string(rc)}")
+            if ev is not None:
+                ev[li][1].record(stream)
+            src = acts[li]
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    st = sc.sc_last_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {sc.sc_status_string(st)}")
+
+    K = args.steps
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in layers] for _ in range(K)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for k in range(K):
+        flush.fill_(float(k))          # evict L2: outside the per-step events
+        step(ev[k])
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    wall = time.perf_counter() - t0
+    clk = clocks.stop()
+    st = sc.sc_last_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after timed steps: {sc.sc_status_string(st)}")
+
+    layer_ms = [[ev[k][li][0].elapsed_time(ev[k][li][1]) for k in range(K)] for li in range(len(layers))]
+    step_ms = [ev[k][0][0].elapsed_time(ev[k][-1][1]) for k in range(K)]
+    ms_step = sum(step_ms) / K
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+    value = world * flops_step / (ms_step * 1e-3) / 1e9
+    mpix = world * N * H * W / (ms_step * 1e-3) / 1e6
+
+    # dominant kernel: the layer with the largest mean time
+    means = [sum(v) / K for v in layer_ms]
+    dom = max(range(len(layers)), key=lambda i: means[i])
+    Ld = layers[dom]
+    dom_bytes = 4 * (N * H * W * (Ld.cin + Ld.cout) + Ld.w.size + Ld.b.size)
+    achieved_tflops = flops_layer[dom] / (means[dom] * 1e-3) / 1e12
+    src_files = ["stencil_conv2d_fwd_gb300/csrc/conv_general.cuh", "stencil_conv2d_fwd_gb300/csrc/common.cuh",
+                 "stencil_conv2d_fwd_gb300/csrc/conv_general_s3.cu"] if Ld.cin > 1 else \
+                ["stencil_conv2d_fwd_gb300/csrc/conv_c1.cu", "stencil_conv2d_fwd_gb300/csrc/common.cuh"]
+    key = f"conv_{Ld.cin}x{Ld.cout}_{Ld.r}x{Ld.s}_{W}x{H}"
+    traffic = profiled_traffic(key, kernel_source_hash(src_files))
+    roofline = {
+        "kernel": f"conv2d_fwd layer {dom + 1} ({Ld.cin}->{Ld.cout}, {Ld.r}x{Ld.s}, {W}x{H})",
+        "bound": "alu",
+        "achieved": round(achieved_tflops, 3),
+        "peak": round(fp32_peak_tflops, 2),
+        "unit": "TFLOP/s",
+        "frac": round(achieved_tflops / fp32_peak_tflops, 4),
+        "traffic": traffic,
+        "algorithmic_bytes": dom_bytes,
+        "peak_note": (f"FP32 FFMA: {n_sm} SMs x {FP32_LANES_PER_SM} lanes x 2 FLOP x {sm_max_mhz:.0f} MHz "
+                      "(max SM clock of MEASURED_PEAKS.json)"),
+        "layer_ms": [round(m, 4) for m in means],
+    }
+
+    result = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded SplitMix64; He-normal weights)",
+        "config": {"workload": WORKLOAD, "layout": "NHWC", "flops_per_step": flops_step,
+                   "l2": "flushed between steps (256 MiB write outside the timed events)",
+                   "parallelism": f"replicas x{world}"},
+        "mpixel_per_s": round(mpix, 2),
+        "wall_s_timed_region": round(wall, 4),
+        "roofline": roofline,
+        "clocks": clk,
+        "gpu_launches": K * len(layers),
+    }
+
+    # ---- end to end through host buffers (pinned), copies inside the timed region
+    x_host = torch.from_numpy(wl.x.copy()).pin_memory()
+    y_host = torch.empty(N * H * W * layers[-1].cout, dtype=torch.float32).pin_memory()
+    e2e_ms = []
+    for k in range(args.warmup + K):
+        flush.fill_(float(k))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        xd.copy_(x_host, non_blocking=True)
+        step()
+        y_host.copy_(acts[-1], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if k >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_step = sum(e2e_ms) / K
+    result["e2e"] = {"value": round(world * flops_step / (e2e_step * 1e-3) / 1e9, 2), "unit": "GFLOP/s",
+                     "ms_per_step": round(e2e_step, 4),
+                     "h2d_bytes_per_step": x_host.numel() * 4, "d2h_bytes_per_step": y_host.numel() * 4}
+
+    # ---- the five workloads, one line each inside the JSON
+    if not args.no_per_config:
+        result["per_config"] = per_config(sc, S, dev, stream, flush, fp32_peak_tflops, hbm_gbs, hbm_src)
+
+    # ---- measured FP32 FMA rate (context for the nominal peak)
+    result["ffma_probe_tflops"] = ffma_probe(sc, dev, stream, n_sm)
+
+    # ---- oracle on the host cores (rank 0 only)
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(wl, min_seconds=10.0)
+
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result))
+
+
+def time_events(fn, stream, flush, reps, warm=3):
+    import torch
+    for _ in range(warm):
+        flush.fill_(0.0)
+        fn()
+    ts = []
+    for k in range(reps):
+        flush.fill_(float(k))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts), min(ts)
+
+
+def time_graph(fn, stream, launches=100, reps=5):
+    """Per-launch time of `launches` back-to-back calls captured in one CUDA graph."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn(s)
+        torch.cuda.current_stream().synchronize()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(launches):
+                fn(s)
+    torch.cuda.current_stream().wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) / launches)
+    return min(ts)
+
+
+def per_config(sc, S, dev, stream, flush, fp32_tflops, hbm_gbs, hbm_src):
+    import numpy as np
+    import torch
+    out = {}
+
+    def conv_entry(name, n, h, w, L, xin_nhwc, graph=False):
+        xd = torch.from_numpy(np.ascontiguousarray(xin_nhwc)).to(dev)
+        wd = torch.from_numpy(L.w).to(dev)
+        bd = torch.from_numpy(L.b).to(dev)
+        yd = torch.empty(n * h * w * L.cout, device=dev)
+
+        def call(s=None):
+            rc = sc.conv2d_fwd(xd, wd, bd, yd, n, h, w, L.cin, L.cout, L.r, L.s, sc.SC_NHWC, L.act,
+                               s if s is not None else stream)
+            if rc != 0:
+                raise RuntimeError(sc.sc_status_string(rc))
+        med, mn = time_events(call, stream, flush, reps=20)
+        flops = conv_flops(n, h, w, L)
+        byts = 4 * (n * h * w * (L.cin + L.cout) + L.w.size + L.b.size)
+        t_roof = max(flops / (fp32_tflops * 1e12), byts / (hbm_gbs * 1e9))
+        bound = "alu" if flops / (fp32_tflops * 1e12) >= byts / (hbm_gbs * 1e9) else "hbm"
+        e = {"ms_median": round(med, 5), "ms_min": round(mn, 5),
+             "gflops": round(flops / (med * 1e-3) / 1e9, 2),
+             "mpixel_per_s": round(n * h * w / (med * 1e-3) / 1e6, 2),
+             "roofline_bound": bound, "roofline_us": round(t_roof * 1e6, 3),
+             "roofline_frac": round(t_roof / (med * 1e-3), 4)}
+        if graph:
+            per = time_graph(call, stream)
+            e["graph_ms_per_launch"] = round(per, 5)
+            e["graph_roofline_frac"] = round(t_roof / (per * 1e-3), 4)
+        out[name] = e
+        return yd
+
+    c1 = S.config(1)
+    conv_entry("1: 64x64 1->1 3x3", 1, 64, 64, c1.layers[0], c1.x[0, 0], graph=True)
+    c2 = S.config(2)
+    conv_entry("2: 128x128 16->16 3x3", 1, 128, 128, c2.layers[0], c2.x.transpose(0, 2, 3, 1), graph=True)
+    c3 = S.config(3)
+    # layers of the net, each timed alone with its real input (the previous layer's output)
+    prev = c3.x[0, 0]
+    for li, L in enumerate(c3.layers):
+        yd = conv_entry(f"3-L{li + 1}: 1280x720 {L.cin}->{L.cout} {L.r}x{L.s}", 1, 720, 1280, L, prev)
+        prev = yd.view(720, 1280, L.cout).cpu().numpy()
+    c4 = S.config(4)
+    conv_entry("4: N=32 56x56 64->64 3x3", 32, 56, 56, c4.layers[0], c4.x.transpose(0, 2, 3, 1))
+
+    c5 = S.config(5)
+    ind = torch.from_numpy(c5.img).to(dev)
+    outd = torch.empty_like(ind)
+
+    def pipe():
+        rc = sc.stencil_pipeline_fwd(ind, outd, c5.h, c5.w, stream)
+        if rc != 0:
+            raise RuntimeError(sc.sc_status_string(rc))
+    med, mn = time_events(pipe, stream, flush, reps=20)
+    byts = 8 * c5.h * c5.w
+    t_roof = byts / (hbm_gbs * 1e9)
+    out["5: 4096x4096 fused blur/unsharp"] = {
+        "ms_median": round(med, 5), "ms_min": round(mn, 5),
+        "mpixel_per_s": round(c5.h * c5.w / (med * 1e-3) / 1e6, 2),
+        "gbytes_per_s": round(byts / (med * 1e-3) / 1e9, 1),
+        "roofline_bound": "hbm", "roofline_us": round(t_roof * 1e6, 3),
+        "roofline_frac": round(t_roof / (med * 1e-3), 4)}
+    out["_peaks"] = {"fp32_tflops": round(fp32_tflops, 2), "hbm_gbs": hbm_gbs, "hbm_source": hbm_src,
+                     "fp32_source": "nominal: SMs x 128 FP32 lanes x 2 x max SM clock"}
+    return out
+
+
+def ffma_probe(sc, dev, stream, n_sm):
+    import torch
+    blocks, iters = n_sm * 8, 4096
+    sink = torch.empty(blocks * 256, device=dev)
+    for _ in range(2):
+        sc.check(sc.sc_measure_ffma_peak(sink, blocks, iters, stream))
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        sc.check(sc.sc_measure_ffma_peak(sink, blocks, iters, stream))
+        e1.record(stream)
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    return round(blocks * 256 * iters * 16 * 2 / (best * 1e-3) / 1e12, 2)
+
+
+# --------------------------------------------------------------------------
+# CPU oracle timing (our arm's cpu_baseline, and the reference arm)
+# --------------------------------------------------------------------------
+
+
+def oracle_net_pass(oracle, wl, rows):
+    """The oracle's forward pass of the net over a strip of `rows` image rows
+    (the strip treated as a rows x 1280 image: the same per-pixel work)."""
+    x = wl.x[:, :, :rows, :]
+    for L in wl.layers:
+        y, _ = oracle.conv2d_nchw(x, L.w, L.b, L.act, with_scale=False)
+        x = y.astype("float32")
+    return wl.n * rows * wl.w
+
+
+def cpu_baseline(wl, min_seconds=10.0, rows=None):
+    import oracle
+    cores = oracle.set_threads(0)
+    rows = rows or wl.h
+    flops_px = sum(2 * L.cin * L.cout * L.r * L.s for L in wl.layers)
+    t0 = time.perf_counter()
+    px = 0
+    passes = 0
+    while True:
+        px += oracle_net_pass(oracle, wl, rows)
+        passes += 1
+        if time.perf_counter() - t0 >= min_seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(px * flops_px / dt / 1e9, 3), "unit": "GFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{passes} pass(es) of the 3-layer net over {rows} of 720 rows x 1280 (fp64 C oracle, "
+                      f"OpenMP), {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import synthetic as S
+    import oracle
+    wl = S.config(3)
+    cores = oracle.set_threads(0)
+    rows = 90                               # one eighth of the image per step
+    flops_px = sum(2 * L.cin * L.cout * L.r * L.s for L in wl.layers)
+    for _ in range(args.warmup):
+        oracle_net_pass(oracle, wl, rows)
+    ts = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        px = oracle_net_pass(oracle, wl, rows)
+        ts.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(ts) / len(ts)
+    value = px * flops_px / (ms * 1e-3) / 1e9
+    sample = f"a {rows}-row strip (of 720) x 1280 of the 3-layer net per step, fp64 C oracle on {cores} threads"
+    print(json.dumps({
+        "metric": METRIC, "value": round(value, 3), "unit": "GFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded SplitMix64; He-normal weights)",
+        "config": {"workload": WORKLOAD, "layout": "NCHW (oracle)", "sample_rows": rows},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 3), "unit": "GFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "GFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,129 @@
+/*
+ * stencilconv: direct 2-D convolution forward pass and a fused
+ * blur/unsharp stencil pipeline on NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of libstencilconv.so.  Plain pointers and sizes only.
+ *
+ * Common conventions
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller; the
+ *    library never frees or keeps it past the call's stream work.
+ *  - Calls are asynchronous on `stream` (NULL = the legacy default stream)
+ *    and return once the work is enqueued.  A nonzero return means nothing
+ *    was enqueued (argument errors) or a launch failed (SC_ERR_CUDA).
+ *  - Arguments are validated on the host before any launch; there is no CPU
+ *    fallback.
+ *  - All data is fp32.  Sizes are ints; element offsets are computed in
+ *    64-bit, so tensors may exceed 2^31 elements as long as each size fits.
+ */
+#ifndef STENCILCONV_H
+#define STENCILCONV_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;                     /* = cudaStream_t's target type */
+typedef struct CUstream_st *sc_stream_t;
+
+typedef enum {
+    SC_OK = 0,
+    SC_ERR_NULL = -1,            /* a required pointer is NULL */
+    SC_ERR_SHAPE = -2,           /* a size is < 1, or the sizes overflow */
+    SC_ERR_UNSUPPORTED = -3,     /* valid convolution the library does not run */
+    SC_ERR_ALIGN = -4,           /* a pointer is not 16-byte aligned */
+    SC_ERR_ALIAS = -5,           /* output overlaps an input */
+    SC_ERR_CUDA = -6,            /* a CUDA call failed; see sc_last_cuda_error */
+    SC_ERR_DEVICE_TIMEOUT = -7   /* a device-side bounded wait gave up */
+} sc_status;
+
+typedef enum { SC_NCHW = 0, SC_NHWC = 1 } sc_layout;
+typedef enum { SC_ACT_NONE = 0, SC_ACT_RELU = 1 } sc_act;
+
+/*
+ * conv2d_fwd: y = act(conv(x, w) + b), stride 1, zero "same" padding.
+ *
+ * Operation ("Optimizing convolution kernels - CNNs in Vulkan Part 2/3",
+ * section "Where we left off"; "Optimizing Memory Efficiency for
+ * Convolution Kernels on Kepler GPUs", Section 3):
+ *   y[n][h][w][co] = act( b[co] + sum_{ci<Cin} sum_{r<R} sum_{s<S}
+ *                          X(n, h + r - R/2, w + s - S/2, ci) * w[co][ci][r][s] )
+ * where X is x inside the image and 0 outside.  This is cross-correlation
+ * (weights are not flipped).  act = ReLU is max(v, 0).
+ *
+ * x : N*H*W*Cin floats, layout `layout` (SC_NHWC: [N][H][W][Cin];
+ *     SC_NCHW: [N][Cin][H][W]).
+ * w : Cout*Cin*R*S floats, always [Cout][Cin][R][S] (OIHW), row-major.
+ * b : Cout floats, or NULL for no bias.
+ * y : N*H*W*Cout floats, same layout as x.  Must not overlap x, w or b.
+ * R, S : odd, 1..7.
+ * Supported: Cin == 1 with Cout == 1 or Cout % 4 == 0; Cin % 4 == 0 with
+ *   Cout % 4 == 0.  x and y 16-byte aligned for Cin > 1 (NHWC vectors of 4
+ *   channels).  Anything else returns SC_ERR_UNSUPPORTED / SC_ERR_ALIGN.
+ * SC_NCHW with more than one channel on either side goes through the
+ *   repack kernels and a stream-ordered temporary buffer (cudaMallocAsync on
+ *   `stream`, freed on `stream` after use).
+ * Returns SC_OK or a negative sc_status.
+ */
+int conv2d_fwd(const float *x, const float *w, const float *b, float *y,
+               int N, int H, int W, int Cin, int Cout, int R, int S,
+               int layout, int act, sc_stream_t stream);
+
+/*
+ * stencil_pipeline_fwd: three stencil stages fused in one pass over a
+ * single-channel image ("Model-Based Warp Overlapped Tiling for Image
+ * Processing Programs on GPUs", Abstract: stages fused into overlapped
+ * warp-sized tiles):
+ *   t1[y][x] = sum_{k=-2..2} c_k in[y][clamp(x+k, 0, W-1)]
+ *   t2[y][x] = sum_{k=-2..2} c_k t1[clamp(y+k, 0, H-1)][x]
+ *   out      = min(max(in + 1.5 (in - t2), 0), 1),   c = (1,4,6,4,1)/16.
+ * in, out : H*W floats, row-major with pitch W; must not overlap.
+ * The intermediates t1 and t2 never leave the chip.
+ * Returns SC_OK or a negative sc_status.
+ */
+int stencil_pipeline_fwd(const float *in, float *out, int H, int W, sc_stream_t stream);
+
+/*
+ * sc_repack: change activation layout between NCHW and NHWC
+ * ("Optimizing convolution kernels - CNNs in Vulkan Part 2/3", section
+ * "Vectorization": the channels of one pixel stored next to each other so
+ * a thread moves four of them as one 16-byte vector).
+ * src, dst : N*C*H*W floats, device, non-overlapping.
+ * src_layout, dst_layout : SC_NCHW or SC_NHWC; equal layouts copy.
+ * Returns SC_OK or a negative sc_status.
+ */
+int sc_repack(const float *src, float *dst, int N, int C, int H, int W,
+              int src_layout, int dst_layout, sc_stream_t stream);
+
+/*
+ * sc_last_device_status: synchronize `stream`, then return and clear the
+ * device-side status word of the current device (SC_OK, or
+ * SC_ERR_DEVICE_TIMEOUT when a kernel's bounded wait expired).  Returns
+ * SC_ERR_CUDA if the synchronization itself failed.
+ */
+int sc_last_device_status(sc_stream_t stream);
+
+/* sc_status_string: static English text for a status code (never NULL). */
+const char *sc_status_string(int status);
+
+/* sc_last_cuda_error: the cudaError_t value behind the last SC_ERR_CUDA
+ * returned on this host thread (0 if none). */
+int sc_last_cuda_error(void);
+
+/*
+ * sc_measure_ffma_peak: measurement helper, not part of the operation.
+ * Runs `blocks` CTAs of 256 threads, each thread doing `iters` iterations
+ * of 16 independent fp32 FMA chains (32 FLOP per chain step), and writes
+ * one float per thread to `sink` (device, blocks*256 floats) so nothing is
+ * optimised away.  Time it on `stream` to measure the FP32 FFMA rate.
+ * Returns SC_OK or a negative sc_status.
+ */
+int sc_measure_ffma_peak(float *sink, int blocks, int iters, sc_stream_t stream);
+
+/* sc_version: library version as 10000*major + 100*minor + patch. */
+int sc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* STENCILCONV_H */

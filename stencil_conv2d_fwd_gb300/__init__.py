@@ -1,0 +1,136 @@
+"""Python binding of libstencilconv.so (direct conv2d forward + fused stencil).
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+The functions below carry the C-ABI names of ``include/stencilconv.h`` and
+return its status codes.  Tensor arguments may be torch tensors (their
+``data_ptr()`` is passed) or raw integer device addresses; ``stream`` may be
+a ``torch.cuda.Stream``, a raw ``cudaStream_t`` integer, or None for torch's
+current stream.
+
+The shared library is built in-tree by ``_build.build()``; if it cannot be
+loaded, ``load()`` raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from . import _build
+
+SC_OK = 0
+SC_ERR_NULL = -1
+SC_ERR_SHAPE = -2
+SC_ERR_UNSUPPORTED = -3
+SC_ERR_ALIGN = -4
+SC_ERR_ALIAS = -5
+SC_ERR_CUDA = -6
+SC_ERR_DEVICE_TIMEOUT = -7
+SC_NCHW = 0
+SC_NHWC = 1
+SC_ACT_NONE = 0
+SC_ACT_RELU = 1
+
+# Every symbol include/stencilconv.h declares, with (restype, argtypes).
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+SIGNATURES = {
+    "conv2d_fwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
+    "stencil_pipeline_fwd": (_I, [_P, _P, _I, _I, _P]),
+    "sc_repack": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "sc_last_device_status": (_I, [_P]),
+    "sc_status_string": (ctypes.c_char_p, [_I]),
+    "sc_last_cuda_error": (_I, []),
+    "sc_measure_ffma_peak": (_I, [_P, _I, _I, _P]),
+    "sc_version": (_I, []),
+}
+
+_lib = None
+
+
+class StencilConvError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        msg = f"{what}: " if what else ""
+        super().__init__(f"{msg}status {status} ({status_string(status)})")
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_stale: bool = True):
+    """Load libstencilconv.so (building it first when sources are newer)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if build_if_stale and _build.is_stale():
+        _build.build()
+    if not os.path.exists(_build.LIB):
+        raise RuntimeError(f"libstencilconv.so is missing at {_build.LIB}; run the build first")
+    lib = ctypes.CDLL(_build.LIB)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(s) -> Optional[int]:
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def conv2d_fwd(x, w, b, y, N, H, W, Cin, Cout, R, S, layout=SC_NHWC, act=SC_ACT_NONE, stream=None) -> int:
+    return load().conv2d_fwd(_ptr(x), _ptr(w), _ptr(b), _ptr(y), N, H, W, Cin, Cout, R, S,
+                             layout, act, _stream(stream))
+
+
+def stencil_pipeline_fwd(inp, out, H, W, stream=None) -> int:
+    return load().stencil_pipeline_fwd(_ptr(inp), _ptr(out), H, W, _stream(stream))
+
+
+def sc_repack(src, dst, N, C, H, W, src_layout, dst_layout, stream=None) -> int:
+    return load().sc_repack(_ptr(src), _ptr(dst), N, C, H, W, src_layout, dst_layout, _stream(stream))
+
+
+def sc_last_device_status(stream=None) -> int:
+    return load().sc_last_device_status(_stream(stream))
+
+
+def sc_status_string(status: int) -> str:
+    return load().sc_status_string(int(status)).decode()
+
+
+status_string = sc_status_string
+
+
+def sc_last_cuda_error() -> int:
+    return load().sc_last_cuda_error()
+
+
+def sc_measure_ffma_peak(sink, blocks, iters, stream=None) -> int:
+    return load().sc_measure_ffma_peak(_ptr(sink), blocks, iters, _stream(stream))
+
+
+def sc_version() -> int:
+    return load().sc_version()
+
+
+def check(status: int, what: str = "") -> None:
+    """Raise StencilConvError for a nonzero status."""
+    if status != SC_OK:
+        raise StencilConvError(status, what)

@@ -1,0 +1,218 @@
+// C-ABI of libstencilconv.so: argument validation, dispatch to the kernels,
+// the NCHW path through a stream-ordered temporary buffer, and the device
+// status word.  Declarations and contracts: include/stencilconv.h.
+#include <cstdint>
+#include <cstring>
+#include <initializer_list>
+
+#include "../../include/stencilconv.h"
+#include "launch.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+// Device-side status word (one per device that loads the library).
+// Kernels with bounded waits record SC_ERR_DEVICE_TIMEOUT here instead of
+// hanging; sc_last_device_status reads and clears it.
+__device__ int g_device_status;
+
+int cuda_fail(cudaError_t e)
+{
+    g_last_cuda_error = (int)e;
+    return SC_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void *a, size_t abytes, const void *b, size_t bbytes)
+{
+    if (!a || !b || abytes == 0 || bbytes == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
+// n = product of the sizes, or -1 if any is < 1 or the product would exceed
+// 2^62 elements.
+long long checked_count(std::initializer_list<int> dims)
+{
+    long long n = 1;
+    for (int d : dims) {
+        if (d < 1) return -1;
+        if (n > (1LL << 62) / d) return -1;
+        n *= d;
+    }
+    return n;
+}
+
+int launch_conv_nhwc(const sc::ConvArgs &a, cudaStream_t st)
+{
+    cudaError_t e;
+    if (a.Cin == 1) {
+        e = sc::launch_conv_c1(a, st);
+    } else {
+        switch (a.S) {
+        case 1: e = sc::launch_conv_general_s1(a, st); break;
+        case 3: e = sc::launch_conv_general_s3(a, st); break;
+        case 5: e = sc::launch_conv_general_s5(a, st); break;
+        case 7: e = sc::launch_conv_general_s7(a, st); break;
+        default: return SC_ERR_UNSUPPORTED;
+        }
+    }
+    return e == cudaSuccess ? SC_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+namespace sc {
+
+int device_sm_count()
+{
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        n = 148;
+    if (dev >= 0 && dev < 64) cached[dev] = n;
+    return n;
+}
+
+}  // namespace sc
+
+extern "C" {
+
+int conv2d_fwd(const float *x, const float *w, const float *b, float *y, int N, int H, int W,
+               int Cin, int Cout, int R, int S, int layout, int act, sc_stream_t stream)
+{
+    if (!x || !w || !y) return SC_ERR_NULL;
+    const long long nx = checked_count({N, H, W, Cin});
+    const long long ny = checked_count({N, H, W, Cout});
+    const long long nw = checked_count({Cout, Cin, R, S});
+    if (nx < 0 || ny < 0 || nw < 0) return SC_ERR_SHAPE;
+    if (H > (1 << 30) || W > (1 << 30)) return SC_ERR_SHAPE;
+    if ((R & 1) == 0 || (S & 1) == 0 || R > 7 || S > 7) return SC_ERR_UNSUPPORTED;
+    if (layout != SC_NCHW && layout != SC_NHWC) return SC_ERR_UNSUPPORTED;
+    if (act != SC_ACT_NONE && act != SC_ACT_RELU) return SC_ERR_UNSUPPORTED;
+    if (Cin == 1) {
+        if (Cout != 1 && (Cout % 4) != 0) return SC_ERR_UNSUPPORTED;
+    } else {
+        if ((Cin % 4) != 0 || (Cout % 4) != 0) return SC_ERR_UNSUPPORTED;
+    }
+    if (Cin > 1 && !aligned16(x)) return SC_ERR_ALIGN;
+    if (Cout > 1 && !aligned16(y)) return SC_ERR_ALIGN;
+    const size_t ybytes = (size_t)ny * sizeof(float);
+    if (overlaps(y, ybytes, x, (size_t)nx * sizeof(float)) ||
+        overlaps(y, ybytes, w, (size_t)nw * sizeof(float)) ||
+        overlaps(y, ybytes, b, b ? (size_t)Cout * sizeof(float) : 0))
+        return SC_ERR_ALIAS;
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    sc::ConvArgs a{x, w, b, y, N, H, W, Cin, Cout, R, S, act};
+    const bool need_in = (layout == SC_NCHW) && Cin > 1;
+    const bool need_out = (layout == SC_NCHW) && Cout > 1;
+    if (!need_in && !need_out) return launch_conv_nhwc(a, st);
+
+    // NCHW with channels: repack to NHWC in a stream-ordered temporary buffer.
+    const size_t in_bytes = need_in ? (size_t)nx * sizeof(float) : 0;
+    const size_t out_bytes = need_out ? (size_t)ny * sizeof(float) : 0;
+    const size_t off = (in_bytes + 255) & ~(size_t)255;
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocAsync(&ws, off + out_bytes, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    float *x_nhwc = need_in ? static_cast<float *>(ws) : nullptr;
+    float *y_nhwc = need_out ? reinterpret_cast<float *>(static_cast<char *>(ws) + off) : y;
+    int rc = SC_OK;
+    if (need_in) {
+        e = sc::launch_transpose_batched(x, x_nhwc, N, Cin, (long long)H * W, st);
+        if (e != cudaSuccess) rc = cuda_fail(e);
+        a.x = x_nhwc;
+    }
+    if (rc == SC_OK) {
+        a.y = y_nhwc;
+        rc = launch_conv_nhwc(a, st);
+    }
+    if (rc == SC_OK && need_out) {
+        e = sc::launch_transpose_batched(y_nhwc, y, N, (long long)H * W, Cout, st);
+        if (e != cudaSuccess) rc = cuda_fail(e);
+    }
+    cudaError_t ef = cudaFreeAsync(ws, st);
+    if (rc == SC_OK && ef != cudaSuccess) rc = cuda_fail(ef);
+    return rc;
+}
+
+int stencil_pipeline_fwd(const float *in, float *out, int H, int W, sc_stream_t stream)
+{
+    if (!in || !out) return SC_ERR_NULL;
+    const long long n = checked_count({H, W});
+    if (n < 0) return SC_ERR_SHAPE;
+    if (overlaps(in, (size_t)n * sizeof(float), out, (size_t)n * sizeof(float))) return SC_ERR_ALIAS;
+    cudaError_t e = sc::launch_stencil_pipeline(in, out, H, W, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SC_OK : cuda_fail(e);
+}
+
+int sc_repack(const float *src, float *dst, int N, int C, int H, int W, int src_layout,
+              int dst_layout, sc_stream_t stream)
+{
+    if (!src || !dst) return SC_ERR_NULL;
+    const long long n = checked_count({N, C, H, W});
+    if (n < 0) return SC_ERR_SHAPE;
+    if ((src_layout != SC_NCHW && src_layout != SC_NHWC) ||
+        (dst_layout != SC_NCHW && dst_layout != SC_NHWC))
+        return SC_ERR_UNSUPPORTED;
+    if (overlaps(src, (size_t)n * sizeof(float), dst, (size_t)n * sizeof(float))) return SC_ERR_ALIAS;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (src_layout == dst_layout || C == 1)
+        e = cudaMemcpyAsync(dst, src, (size_t)n * sizeof(float), cudaMemcpyDeviceToDevice, st);
+    else if (src_layout == SC_NCHW)
+        e = sc::launch_transpose_batched(src, dst, N, C, (long long)H * W, st);
+    else
+        e = sc::launch_transpose_batched(src, dst, N, (long long)H * W, C, st);
+    return e == cudaSuccess ? SC_OK : cuda_fail(e);
+}
+
+int sc_last_device_status(sc_stream_t stream)
+{
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    int v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (v != 0) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int));
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return v;
+}
+
+const char *sc_status_string(int status)
+{
+    switch (status) {
+    case SC_OK: return "ok";
+    case SC_ERR_NULL: return "a required pointer is NULL";
+    case SC_ERR_SHAPE: return "a size is < 1 or the sizes overflow";
+    case SC_ERR_UNSUPPORTED: return "unsupported convolution parameters";
+    case SC_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case SC_ERR_ALIAS: return "output overlaps an input";
+    case SC_ERR_CUDA: return "a CUDA call failed";
+    case SC_ERR_DEVICE_TIMEOUT: return "a device-side bounded wait expired";
+    default: return "unknown status";
+    }
+}
+
+int sc_last_cuda_error(void) { return g_last_cuda_error; }
+
+int sc_measure_ffma_peak(float *sink, int blocks, int iters, sc_stream_t stream)
+{
+    if (!sink) return SC_ERR_NULL;
+    if (blocks < 1 || iters < 1 || blocks > (1 << 24)) return SC_ERR_SHAPE;
+    cudaError_t e = sc::launch_ffma_peak(sink, blocks, iters, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SC_OK : cuda_fail(e);
+}
+
+int sc_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,319 @@
+// Special-case direct convolution: one input channel.
+//
+// Method: "Optimizing Memory Efficiency for Convolution Kernels on Kepler
+// GPUs", Section 3.2 (special case) and Algorithm 1:
+//  * a CTA owns a block of image columns and a band of rows; its threads
+//    sweep the band downward one output row per step (Fig. 5a);
+//  * vertical reuse lives in registers: each thread keeps the K input rows
+//    its outputs need and loads one new row per step (Algorithm 1, lines
+//    3-6);
+//  * each thread computes n = 4 contiguous output pixels and reads them as
+//    one 16-byte unit (Section 3.2.3, Fig. 5b: W_CD matched to W_SMB);
+//  * every thread of a warp reads the same filter tap at the same time, so
+//    filter reads are broadcasts (Section 3.2.2 puts them in constant
+//    memory; here the CTA stages them once in shared memory, which gives
+//    the same broadcast without a per-call constant-bank upload).
+// Horizontal sharing between neighbouring threads goes through warp
+// shuffles instead of a shared-memory row: a lane's left and right halo
+// pixels are the edge values its neighbour lanes already hold in registers;
+// only the two outermost pixel lanes of a warp load their halo from global.
+//
+// Output channels: each thread computes F_T of them for its 4 pixels;
+// CL lanes of a warp split a group of CL*F_T channels (F_T = 8: channels
+// g*4*CL + 4*cl + e, g in {0,1}) so one warp store writes 4*CL contiguous
+// NHWC channels of each of its pixels.  Filters of an R x S kernel sit centred in a
+// K x K register window (K = max(R, S), zero taps around them).
+#include "common.cuh"
+#include "launch.h"
+
+namespace sc {
+
+template <int K, int F_T, int CL_>
+struct C1Cfg {
+    static constexpr int CL = CL_;              // lanes along output channels
+    static constexpr int PL = 32 / CL;          // pixel lanes per warp
+    static constexpr int HALO = K / 2;
+    static constexpr int WIN = 4 + K - 1;       // pixels a thread needs per row
+    static constexpr int CO_CTA = F_T * CL;     // output channels per CTA
+    static constexpr int NG = F_T >= 4 ? F_T / 4 : 1;
+    static_assert(HALO <= 4, "halo must come from the adjacent lane");
+};
+
+// Raw loads of one input row for this thread (Algorithm 1's register
+// prefetch): the 4 own pixels x0..x0+3 and, for the two outermost pixel
+// lanes of the warp, their halo pixels.  Zero outside the image.
+struct C1Raw {
+    float own[4];
+    float edge[4];  // halo pixels loaded from global (outermost lanes only)
+};
+
+__device__ __forceinline__ float ldg_nc_f32(const float *p)
+{
+    float v;
+    asm volatile("ld.global.nc.f32 %0, [%1];\n" : "=f"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float4 ldg_nc_f32x4(const float *p)
+{
+    float4 v;
+    asm volatile("ld.global.nc.v4.f32 {%0,%1,%2,%3}, [%4];\n"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+template <class C>
+__device__ __forceinline__ void c1_issue_row(C1Raw &raw, const float *__restrict__ xrow, bool row_ok,
+                                             int x0, int W, bool vec, int pl)
+{
+#pragma unroll
+    for (int j = 0; j < 4; ++j) raw.own[j] = 0.f;
+#pragma unroll
+    for (int h = 0; h < 4; ++h) raw.edge[h] = 0.f;
+    if (!row_ok) return;
+    if (vec && x0 + 3 < W) {
+        const float4 t = ldg_nc_f32x4(xrow + x0);
+        raw.own[0] = t.x; raw.own[1] = t.y; raw.own[2] = t.z; raw.own[3] = t.w;
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (x0 + j < W) raw.own[j] = ldg_nc_f32(xrow + x0 + j);
+    }
+    if (pl == 0) {
+#pragma unroll
+        for (int h = 0; h < C::HALO; ++h) {
+            const int gx = x0 - C::HALO + h;
+            if (gx >= 0 && gx < W) raw.edge[h] = ldg_nc_f32(xrow + gx);
+        }
+    } else if (pl == C::PL - 1) {
+#pragma unroll
+        for (int h = 0; h < C::HALO; ++h) {
+            const int gx = x0 + 4 + h;
+            if (gx < W) raw.edge[h] = ldg_nc_f32(xrow + gx);
+        }
+    }
+}
+
+// Window of one row: win[0..WIN) = x[row][x0 - HALO .. x0 + 3 + HALO].  The
+// halo pixels are the neighbour lanes' own pixels, passed by shuffle.
+template <class C>
+__device__ __forceinline__ void c1_finish_row(float (&win)[C::WIN], const C1Raw &raw, int pl,
+                                              int lane)
+{
+#pragma unroll
+    for (int j = 0; j < 4; ++j) win[C::HALO + j] = raw.own[j];
+    if constexpr (C::HALO > 0) {
+        const int left = lane - C::CL;    // neighbour lane to the left (same channels)
+        const int right = lane + C::CL;
+#pragma unroll
+        for (int h = 0; h < C::HALO; ++h) {
+            // left halo pixel x0 - HALO + h is the left neighbour's own[4 - HALO + h]
+            const float l = __shfl_sync(0xffffffffu, raw.own[4 - C::HALO + h], left < 0 ? lane : left);
+            // right halo pixel x0 + 4 + h is the right neighbour's own[h]
+            const float r = __shfl_sync(0xffffffffu, raw.own[h], right > 31 ? lane : right);
+            win[h] = pl == 0 ? raw.edge[h] : l;
+            win[C::HALO + 4 + h] = pl == C::PL - 1 ? raw.edge[h] : r;
+        }
+    }
+}
+
+template <int K, int F_T, int CL>
+__global__ void __launch_bounds__(256)
+    conv_c1_kernel(const float *__restrict__ x, const float *__restrict__ w,
+                   const float *__restrict__ bias, float *__restrict__ y, int N, int H, int W,
+                   int Cout, int R, int S, int act, int rows_per_cta, int col_tiles, int vec)
+{
+    using C = C1Cfg<K, F_T, CL>;
+    __shared__ __align__(16) float ws[K * K * C::CO_CTA];
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const int cl = lane % CL;
+    const int pl = lane / CL;
+    const int co0 = blockIdx.y * C::CO_CTA;
+    const int n = blockIdx.z;
+    const int ct = blockIdx.x % col_tiles;
+    const int rt = blockIdx.x / col_tiles;
+    const int x0 = (ct * nwarps + warp) * (C::PL * 4) + pl * 4;
+    const int y0 = rt * rows_per_cta;
+    const int y1 = min(H, y0 + rows_per_cta);
+
+    // Stage the CTA's filters as [K*K taps][CO_CTA], centred, zero elsewhere.
+    for (int e = tid; e < K * K * C::CO_CTA; e += blockDim.x) {
+        const int col = e % C::CO_CTA;
+        const int tap = e / C::CO_CTA;
+        const int r = tap / K - (K - R) / 2;
+        const int s = tap % K - (K - S) / 2;
+        const int co = co0 + col;
+        float v = 0.f;
+        if (r >= 0 && r < R && s >= 0 && s < S && co < Cout) v = w[((long long)co * R + r) * S + s];
+        ws[e] = v;
+    }
+    __syncthreads();
+
+    // this thread's output channels (CTA-local), and their bias
+    int col_of[F_T];
+#pragma unroll
+    for (int f = 0; f < F_T; ++f)
+        col_of[f] = F_T >= 4 ? (f / 4) * (4 * CL) + 4 * cl + (f % 4) : cl * F_T + f;
+    float bv[F_T];
+#pragma unroll
+    for (int f = 0; f < F_T; ++f) {
+        const int co = co0 + col_of[f];
+        bv[f] = (bias && co < Cout) ? bias[co] : 0.f;
+    }
+
+    const float *xn = x + (long long)n * H * W;
+    float win[K][C::WIN];
+    // prologue: rows y0 - HALO .. y0 + HALO - 1 into window rows 0 .. K-2
+#pragma unroll
+    for (int t = 0; t < K - 1; ++t) {
+        const int yy = y0 - C::HALO + t;
+        const bool ok = yy >= 0 && yy < H;
+        C1Raw raw;
+        c1_issue_row<C>(raw, xn + (long long)(ok ? yy : 0) * W, ok, x0, W, vec, pl);
+        c1_finish_row<C>(win[t], raw, pl, lane);
+    }
+
+    for (int oy = y0; oy < y1; ++oy) {
+        // prefetch the new bottom row (oy + HALO) into registers
+        C1Raw raw;
+        {
+            const int yy = oy + C::HALO;
+            const bool ok = yy < H;
+            c1_issue_row<C>(raw, xn + (long long)(ok ? yy : 0) * W, ok, x0, W, vec, pl);
+        }
+        float acc[F_T][4];
+#pragma unroll
+        for (int f = 0; f < F_T; ++f)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[f][j] = 0.f;
+        // kernel rows 0 .. K-2 use rows already in registers; the last
+        // kernel row uses the prefetched row once its halo is exchanged
+#pragma unroll
+        for (int ky = 0; ky < K; ++ky) {
+            if (ky == K - 1) c1_finish_row<C>(win[ky], raw, pl, lane);
+            // keep one kernel row of filter loads in flight at a time
+            asm volatile("" ::: "memory");
+#pragma unroll
+            for (int kx = 0; kx < K; ++kx) {
+                const float *wt = ws + (ky * K + kx) * C::CO_CTA;
+                float wv[F_T];
+                if constexpr (F_T >= 4) {
+#pragma unroll
+                    for (int g = 0; g < F_T / 4; ++g) {
+                        const float4 t = *reinterpret_cast<const float4 *>(wt + g * 4 * CL + 4 * cl);
+                        wv[4 * g + 0] = t.x;
+                        wv[4 * g + 1] = t.y;
+                        wv[4 * g + 2] = t.z;
+                        wv[4 * g + 3] = t.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int f = 0; f < F_T; ++f) wv[f] = wt[cl * F_T + f];
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float v = win[ky][j + kx];
+#pragma unroll
+                    for (int f = 0; f < F_T; ++f) acc[f][j] = fmaf(wv[f], v, acc[f][j]);
+                }
+            }
+        }
+        // epilogue
+        float *yrow = y + ((long long)n * H + oy) * W * Cout;
+        if constexpr (F_T >= 4) {
+#pragma unroll
+            for (int g = 0; g < F_T / 4; ++g) {
+                const int co = co0 + g * 4 * CL + 4 * cl;
+                if (co < Cout) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if (x0 + j < W) {
+                            float4 o;
+                            o.x = relu_if(acc[4 * g + 0][j] + bv[4 * g + 0], act);
+                            o.y = relu_if(acc[4 * g + 1][j] + bv[4 * g + 1], act);
+                            o.z = relu_if(acc[4 * g + 2][j] + bv[4 * g + 2], act);
+                            o.w = relu_if(acc[4 * g + 3][j] + bv[4 * g + 3], act);
+                            *reinterpret_cast<float4 *>(yrow + (long long)(x0 + j) * Cout + co) = o;
+                        }
+                    }
+                }
+            }
+        } else {
+            // F_T == 1 (Cout == 1): four contiguous pixels of one channel
+            if (co0 + cl < Cout) {
+                float o[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) o[j] = relu_if(acc[0][j] + bv[0], act);
+                if (vec && x0 + 3 < W) {
+                    *reinterpret_cast<float4 *>(yrow + x0) = make_float4(o[0], o[1], o[2], o[3]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (x0 + j < W) yrow[x0 + j] = o[j];
+                }
+            }
+        }
+        // slide the register window down one row
+#pragma unroll
+        for (int t = 0; t < K - 1; ++t)
+#pragma unroll
+            for (int j = 0; j < C::WIN; ++j) win[t][j] = win[t + 1][j];
+    }
+}
+
+template <int K, int F_T, int CL>
+static cudaError_t launch_c1_cfg(const ConvArgs &a, cudaStream_t st)
+{
+    using C = C1Cfg<K, F_T, CL>;
+    const int warp_cols = C::PL * 4;
+    const int warps_needed = (a.W + warp_cols - 1) / warp_cols;
+    const int nwarps = warps_needed < 8 ? warps_needed : 8;
+    const int col_tiles = (a.W + nwarps * warp_cols - 1) / (nwarps * warp_cols);
+    const int groups = (a.Cout + C::CO_CTA - 1) / C::CO_CTA;
+    // Enough CTAs for two per SM, but bands of at least 2K rows so the
+    // K - 1 rows of vertical halo stay a small share of each band's loads.
+    const long long per_band = (long long)col_tiles * groups * a.N;
+    const long long want = 2LL * device_sm_count();
+    long long bands = (want + per_band - 1) / per_band;
+    int min_rows = 2 * K;
+    long long max_bands = (a.H + min_rows - 1) / min_rows;
+    if (bands > max_bands) bands = max_bands;
+    if (bands < 1) bands = 1;
+    const int rows_per_cta = (int)((a.H + bands - 1) / bands);
+    const long long nb = (long long)col_tiles * ((a.H + rows_per_cta - 1) / rows_per_cta);
+    if (nb > 0x7fffffffLL || groups > 65535 || a.N > 65535) return cudaErrorInvalidConfiguration;
+    const int vec = ((a.W & 3) == 0) && ((reinterpret_cast<uintptr_t>(a.x) & 15) == 0) &&
+                    ((reinterpret_cast<uintptr_t>(a.y) & 15) == 0);
+    conv_c1_kernel<K, F_T, CL><<<dim3((unsigned)nb, groups, a.N), nwarps * 32, 0, st>>>(
+        a.x, a.w, a.b, a.y, a.N, a.H, a.W, a.Cout, a.R, a.S, a.act, rows_per_cta, col_tiles, vec);
+    return cudaGetLastError();
+}
+
+template <int K>
+static cudaError_t launch_c1_k(const ConvArgs &a, cudaStream_t st)
+{
+    if (a.Cout == 1) return launch_c1_cfg<K, 1, 1>(a, st);
+    if (a.Cout == 4) return launch_c1_cfg<K, 4, 1>(a, st);
+    if (a.Cout <= 8) return launch_c1_cfg<K, 8, 1>(a, st);
+    if (a.Cout <= 16) return launch_c1_cfg<K, 8, 2>(a, st);
+    return launch_c1_cfg<K, 8, 4>(a, st);
+}
+
+cudaError_t launch_conv_c1(const ConvArgs &a, cudaStream_t st)
+{
+    const int K = a.R > a.S ? a.R : a.S;
+    switch (K) {
+    case 1: return launch_c1_k<1>(a, st);
+    case 3: return launch_c1_k<3>(a, st);
+    case 5: return launch_c1_k<5>(a, st);
+    case 7: return launch_c1_k<7>(a, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace sc

@@ -1,0 +1,40 @@
+// Internal launcher interface between the C-ABI layer (api.cu) and the
+// kernel translation units.  Not exported.
+#pragma once
+
+#include <cuda_runtime.h>
+
+namespace sc {
+
+struct ConvArgs {
+    const float *x;   // NHWC activations (Cin == 1: [N][H][W])
+    const float *w;   // OIHW weights
+    const float *b;   // bias or nullptr
+    float *y;         // NHWC output
+    int N, H, W, Cin, Cout, R, S, act;
+};
+
+// General direct convolution, Cin % 4 == 0, Cout % 4 == 0 (conv_general_s*.cu).
+cudaError_t launch_conv_general_s1(const ConvArgs &a, cudaStream_t st);
+cudaError_t launch_conv_general_s3(const ConvArgs &a, cudaStream_t st);
+cudaError_t launch_conv_general_s5(const ConvArgs &a, cudaStream_t st);
+cudaError_t launch_conv_general_s7(const ConvArgs &a, cudaStream_t st);
+
+// Single-input-channel convolution, Cout == 1 or Cout % 4 == 0 (conv_c1.cu).
+cudaError_t launch_conv_c1(const ConvArgs &a, cudaStream_t st);
+
+// Fused blur/unsharp pipeline (stencil.cu).
+cudaError_t launch_stencil_pipeline(const float *in, float *out, int H, int W, cudaStream_t st);
+
+// dst[n][b][a] = src[n][a][b] (repack.cu): NCHW->NHWC is (A=C, B=H*W),
+// NHWC->NCHW is (A=H*W, B=C).
+cudaError_t launch_transpose_batched(const float *src, float *dst, int N, long long A,
+                                     long long B, cudaStream_t st);
+
+// FP32 FMA rate probe (peak.cu).
+cudaError_t launch_ffma_peak(float *sink, int blocks, int iters, cudaStream_t st);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace sc

@@ -1,0 +1,139 @@
+"""Shared-memory layouts of the CUDA kernels: the XOR swizzle they use is a
+bijection, and the warps' access patterns are bank-conflict-free.
+
+The swizzle functions are compiled from the kernels' own header
+(stencil_conv2d_fwd_gb300/csrc/common.cuh) as host C++, so this checks the
+code the kernels run.  The per-lane address patterns restate the thread ->
+pixel maps of conv_general.cuh and repack.cu.  Properties follow "CUDA共有
+メモリのスウィズリング" (section "スウィズリングのプロパティ"): one-to-one, and as
+many distinct banks as possible for the warp's access.
+"""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HDR = os.path.join(ROOT, "stencil_conv2d_fwd_gb300", "csrc", "common.cuh")
+
+
+@pytest.fixture(scope="module")
+def swz(tmp_path_factory):
+    d = tmp_path_factory.mktemp("swz")
+    src = d / "swz.cpp"
+    src.write_text(f'#include "{HDR}"\n'
+                   'extern "C" int h_swz16(int i, int L) { return sc::swz16(i, L); }\n'
+                   'extern "C" int h_swz_col(int r, int c, int L) { return sc::swz_col(r, c, L); }\n')
+    so = d / "libswz.so"
+    subprocess.run(["g++", "-std=c++17", "-O1", "-fPIC", "-shared", str(src), "-o", str(so)], check=True)
+    lib = ctypes.CDLL(str(so))
+    lib.h_swz16.argtypes = [ctypes.c_int, ctypes.c_int]
+    lib.h_swz_col.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    return lib
+
+
+def wavefronts_128bit(chunks):
+    """Shared-memory wavefronts for one warp-wide 16-byte access: distinct
+    16-byte chunks are served 8 per wavefront, at most one per 128-byte bank
+    window position (chunk mod 8)."""
+    uniq = set(chunks)
+    per_pos = {}
+    for c in uniq:
+        per_pos[c % 8] = per_pos.get(c % 8, 0) + 1
+    return max(per_pos.values())
+
+
+def min_wavefronts_128bit(chunks):
+    return -(-len(set(chunks)) // 8)
+
+
+@pytest.mark.parametrize("L", [1, 2, 3, 4, 5])
+def test_swz16_is_a_bijection_per_row(swz, L):
+    n = 1 << L
+    for base in range(0, 64 * n, n):
+        got = sorted(swz.h_swz16(base + k, L) for k in range(n))
+        assert got == list(range(base, base + n))
+
+
+def test_swz16_matches_the_page_formula(swz):
+    """16-byte chunks, 128-byte swizzle rows (T = TC = 16 B, NX = 8):
+    x_swz = (y_chunk XOR x_chunk) mod 8 with y_chunk = i / 8, x_chunk = i mod 8."""
+    for i in range(4096):
+        y, x = divmod(i, 8)
+        assert swz.h_swz16(i, 3) == y * 8 + ((y ^ x) % 8)
+
+
+# (S, F_TB, W_T, TH, TW, C_SH): the tile table of dispatch_general<S>()
+GEN_TABLE = [(64, 8, 8, 32, 8), (32, 8, 8, 64, 8), (16, 4, 4, 64, 8), (8, 4, 4, 128, 8), (4, 8, 4, 256, 8)]
+
+
+def gen_cfg(S, F_TB, W_T, TH, TW, C_SH):
+    F_T = 8 if F_TB >= 8 else 4
+    T_X = F_TB // F_T
+    PXL = 32 // T_X
+    WARP_COLS = PXL * W_T
+    return dict(F_T=F_T, T_X=T_X, PXL=PXL, WARP_COLS=WARP_COLS, WPR=TW // WARP_COLS,
+                NT=(TW // WARP_COLS) * TH * 32, TWP=TW + S - 1, CB=C_SH // 4)
+
+
+@pytest.mark.parametrize("S", [1, 3, 5, 7])
+@pytest.mark.parametrize("F_TB,W_T,TH,TW,C_SH", GEN_TABLE)
+def test_general_conv_pixel_reads_conflict_free(swz, S, F_TB, W_T, TH, TW, C_SH):
+    c = gen_cfg(S, F_TB, W_T, TH, TW, C_SH)
+    R = S
+    THh = TH + R - 1
+    for warp in range(c["NT"] // 32):
+        ry = warp // c["WPR"]
+        for cb in range(c["CB"]):
+            for r in range(R):
+                for j in range(W_T + S - 1):
+                    chunks = []
+                    for lane in range(32):
+                        pl = lane // c["T_X"]
+                        cx0 = (warp % c["WPR"]) * c["WARP_COLS"] + pl * W_T
+                        base = (cb * THh + ry + r) * c["TWP"] + cx0
+                        chunks.append(swz.h_swz16(base + j, 3))
+                    assert wavefronts_128bit(chunks) == min_wavefronts_128bit(chunks), \
+                        (warp, cb, r, j)
+
+
+@pytest.mark.parametrize("S", [1, 3, 5, 7])
+@pytest.mark.parametrize("F_TB,W_T,TH,TW,C_SH", GEN_TABLE)
+def test_general_conv_tile_writes_conflict_free_and_bijective(swz, S, F_TB, W_T, TH, TW, C_SH):
+    c = gen_cfg(S, F_TB, W_T, TH, TW, C_SH)
+    nq = c["CB"] * (TH + S - 1) * c["TWP"]
+    allocated = (nq + 7) // 8 * 8          # GenCfg::in_chunks: padded to whole 8-chunk rows
+    phys = [swz.h_swz16(q, 3) for q in range(nq)]
+    assert len(set(phys)) == nq            # one-to-one
+    assert max(phys) < allocated           # never past the padded tile (the filter slice follows it)
+    for k in range(0, nq, c["NT"]):
+        for w0 in range(k, min(nq, k + c["NT"]), 32):
+            chunks = phys[w0:min(nq, w0 + 32)]
+            assert wavefronts_128bit(chunks) == min_wavefronts_128bit(chunks)
+
+
+def test_general_conv_unswizzled_pixel_reads_would_conflict():
+    """Without the XOR the same warp read puts its pixel lanes W_T chunks apart,
+    so (for W_T = 8) every lane lands on the same bank window position."""
+    W_T, PXL = 8, 4
+    chunks = [pl * W_T for pl in range(PXL) for _ in range(8)]
+    assert wavefronts_128bit(chunks) == PXL > min_wavefronts_128bit(chunks)
+
+
+def bank_ways_32bit(word_addrs):
+    per = {}
+    for a in set(word_addrs):
+        per[a % 32] = per.get(a % 32, 0) + 1
+    return max(per.values())
+
+
+def test_transpose_tile_conflict_free(swz):
+    for ra in range(32):  # row write: lanes along the tile row
+        words = [ra * 32 + swz.h_swz_col(ra, tx, 5) for tx in range(32)]
+        assert bank_ways_32bit(words) == 1
+    for rb in range(32):  # swizzled column read: lane = tile row
+        words = [tx * 32 + swz.h_swz_col(tx, rb, 5) for tx in range(32)]
+        assert bank_ways_32bit(words) == 1
+        plain = [tx * 32 + rb for tx in range(32)]
+        assert bank_ways_32bit(plain) == 32

@@ -1,0 +1,153 @@
+"""conv2d_fwd on the GPU vs the fp64 oracle, element by element.
+
+Tolerance: |y_gpu - y_ref| <= 1e-5 * (sum |x * w| + |b|) per element (the
+fp32 bound of the direct-convolution path).  Covers the five workloads at
+full size (layer by layer for the 3-layer net, each layer fed the GPU's own
+input), ragged tiles, every supported filter size, both layouts, and edge
+cases (images smaller than the filter, one pixel, N > 1, no bias).
+"""
+import numpy as np
+import pytest
+import torch
+
+import synthetic as S
+import stencil_conv2d_fwd_gb300 as sc
+from parity_util import assert_conv_close, conv_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def _one(oracle_mod, dev, x, L, layout=sc.SC_NHWC, rows=None):
+    y = conv_gpu(x, L.w, L.b, L.act, dev, layout=layout)
+    yr, a = oracle_mod.conv2d_nchw(x, L.w, L.b, L.act)
+    return y, yr, a
+
+
+@pytest.mark.parametrize("cid", [1, 2, 4])
+def test_workload_full_size(oracle_mod, cuda_dev, sc, cid):
+    c = S.config(cid)
+    L = c.layers[0]
+    y, yr, a = _one(oracle_mod, cuda_dev, c.x, L)
+    assert_conv_close(y, yr, a, what=f"workload {cid}")
+
+
+def test_upscaling_net_layer_by_layer_and_end_to_end(oracle_mod, cuda_dev, sc):
+    """Each layer is checked against the oracle fed the GPU's own input to it;
+    the final output is also checked against the all-fp64 chain with the
+    propagated bound E_L = 1e-5 A_L + conv(|w_L|, E_{L-1} + u |y_{L-1}|)."""
+    c = S.config(3)
+    x = c.x
+    x64 = c.x.astype(np.float64)
+    E = np.zeros_like(x64)
+    u = 2.0 ** -24
+    for li, L in enumerate(c.layers):
+        y = conv_gpu(x, L.w, L.b, L.act, cuda_dev)
+        yr, a = oracle_mod.conv2d_nchw(x, L.w, L.b, L.act)
+        assert_conv_close(y, yr, a, what=f"layer {li + 1}")
+        # all-fp64 chain: the oracle takes fp32 inputs, so the chain's own
+        # rounding to fp32 between layers enters the bound as u*|y|
+        y64, a64 = oracle_mod.conv2d_nchw(x64.astype(np.float32), L.w, L.b, L.act)
+        Ein = E + u * np.abs(x64) + np.abs(x64 - x64.astype(np.float32).astype(np.float64))
+        prop = torch.nn.functional.conv2d(torch.from_numpy(Ein), torch.from_numpy(np.abs(L.w).astype(np.float64)),
+                                          padding=(L.r // 2, L.s // 2)).numpy()
+        E = 1e-5 * a + prop   # a: scale of this layer at the GPU's own input
+        x, x64 = y, y64
+    err = np.abs(x.astype(np.float64) - x64)
+    assert (err <= E).all(), f"end-to-end error {err.max()} exceeds the propagated bound"
+
+
+SHAPES = [
+    # (N, Cin, Cout, H, W, R, S)
+    (1, 4, 4, 1, 1, 3, 3),
+    (1, 4, 4, 2, 3, 5, 5),
+    (2, 8, 8, 9, 13, 3, 3),
+    (1, 12, 20, 17, 70, 3, 3),
+    (3, 16, 16, 33, 65, 3, 3),
+    (1, 32, 32, 19, 131, 3, 3),
+    (1, 32, 4, 11, 300, 3, 3),
+    (2, 64, 64, 15, 57, 3, 3),
+    (1, 36, 68, 10, 40, 3, 3),
+    (1, 64, 128, 9, 33, 3, 3),
+    (1, 68, 48, 7, 29, 3, 3),
+    (1, 20, 12, 21, 22, 1, 1),
+    (1, 16, 32, 13, 70, 5, 5),
+    (1, 8, 16, 12, 40, 7, 7),
+    (1, 8, 8, 12, 17, 3, 5),
+    (1, 8, 8, 12, 17, 7, 1),
+    (2, 4, 36, 5, 9, 5, 3),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[str(s) for s in SHAPES])
+@pytest.mark.parametrize("act", [0, 1])
+def test_general_shapes(oracle_mod, cuda_dev, sc, shape, act):
+    N, Cin, Cout, H, W, R, S_ = shape
+    c = S.conv_case(100 + Cin + Cout + H, N, Cin, Cout, H, W, R, S_, act=act)
+    L = c.layers[0]
+    y, yr, a = _one(oracle_mod, cuda_dev, c.x, L)
+    assert_conv_close(y, yr, a, what=str(shape))
+
+
+C1_SHAPES = [
+    (1, 1, 1, 1, 3, 3), (1, 1, 2, 3, 5, 5), (1, 1, 64, 64, 3, 3), (2, 1, 37, 45, 3, 3),
+    (1, 4, 20, 33, 5, 5), (1, 8, 31, 130, 5, 5), (1, 12, 9, 17, 3, 3), (1, 16, 40, 70, 7, 7),
+    (1, 24, 16, 100, 5, 5), (1, 32, 50, 260, 5, 5), (2, 32, 23, 41, 3, 3), (1, 64, 12, 66, 5, 5),
+    (1, 32, 10, 35, 1, 1), (1, 8, 15, 21, 3, 7), (1, 1, 64, 1030, 7, 7), (1, 32, 6, 1300, 5, 5),
+]
+
+
+@pytest.mark.parametrize("shape", C1_SHAPES, ids=[str(s) for s in C1_SHAPES])
+def test_single_input_channel_shapes(oracle_mod, cuda_dev, sc, shape):
+    N, Cout, H, W, R, S_ = shape
+    c = S.conv_case(200 + Cout + H + W, N, 1, Cout, H, W, R, S_, act=1)
+    L = c.layers[0]
+    y, yr, a = _one(oracle_mod, cuda_dev, c.x, L)
+    assert_conv_close(y, yr, a, what=str(shape))
+
+
+@pytest.mark.parametrize("shape", [(2, 8, 12, 9, 20, 3, 3), (1, 1, 16, 13, 37, 5, 5), (1, 16, 4, 17, 9, 3, 3),
+                                   (1, 1, 1, 10, 11, 3, 3)])
+def test_nchw_layout(oracle_mod, cuda_dev, sc, shape):
+    N, Cin, Cout, H, W, R, S_ = shape
+    c = S.conv_case(300 + Cin + Cout, N, Cin, Cout, H, W, R, S_, act=1)
+    L = c.layers[0]
+    y, yr, a = _one(oracle_mod, cuda_dev, c.x, L, layout=sc.SC_NCHW)
+    assert_conv_close(y, yr, a, what="nchw " + str(shape))
+
+
+def test_no_bias(oracle_mod, cuda_dev, sc):
+    c = S.conv_case(400, 1, 16, 16, 20, 30, 3, 3, act=0)
+    L = c.layers[0]
+    y = conv_gpu(c.x, L.w, None, 0, cuda_dev)
+    yr, a = oracle_mod.conv2d_nchw(c.x, L.w, None, 0)
+    assert_conv_close(y, yr, a, what="no bias")
+
+
+def test_delta_filter_is_exact(cuda_dev, sc):
+    """A centre delta filter returns x + b exactly (one nonzero product)."""
+    c = S.conv_case(401, 1, 8, 8, 17, 23, 3, 3, act=0)
+    w = np.zeros((8, 8, 3, 3), np.float32)
+    for i in range(8):
+        w[i, i, 1, 1] = 1.0
+    b = np.linspace(-1, 1, 8).astype(np.float32)
+    y = conv_gpu(c.x, w, b, 0, cuda_dev)
+    np.testing.assert_array_equal(y, c.x + b[None, :, None, None])
+
+
+def test_side_stream(oracle_mod, cuda_dev, sc):
+    c = S.conv_case(402, 1, 8, 8, 16, 16, 3, 3, act=1)
+    L = c.layers[0]
+    s = torch.cuda.Stream()
+    y = conv_gpu(c.x, L.w, L.b, 1, cuda_dev, stream=s)
+    yr, a = oracle_mod.conv2d_nchw(c.x, L.w, L.b, 1)
+    assert_conv_close(y, yr, a, what="side stream")
+
+
+def test_misaligned_pointer_rejected_without_launch(cuda_dev, sc):
+    x = torch.zeros(4 * 8 * 8 + 1, device=cuda_dev)
+    w = torch.zeros(4 * 4 * 9, device=cuda_dev)
+    y = torch.full((4 * 8 * 8,), 3.0, device=cuda_dev)
+    rc = sc.conv2d_fwd(x.data_ptr() + 4, w, None, y, 1, 8, 8, 4, 4, 3, 3, sc.SC_NHWC, 0)
+    assert rc == sc.SC_ERR_ALIGN
+    torch.cuda.synchronize()
+    assert (y == 3.0).all()
