@@ -122,6 +122,43 @@ int sc_measure_ffma_peak(float *sink, int blocks, int iters, sc_stream_t stream)
 /* sc_version: library version as 10000*major + 100*minor + patch. */
 int sc_version(void);
 
+/* Floats of device scratch behind conv2d_fwd_nchw_noalloc (32 MiB). */
+#define SC_NOALLOC_SCRATCH_FLOATS (8u * 1024u * 1024u)
+
+/*
+ * conv2d_fwd_nchw_noalloc: conv2d_fwd with layout SC_NCHW, for callers that
+ * must not allocate device memory while they run.  (The pages describe no
+ * such entry point; it has no counterpart there.)
+ *
+ * conv2d_fwd with SC_NCHW and more than one channel repacks through a
+ * temporary buffer it allocates on the stream.  Some callers cannot accept
+ * that: a service that reserved the GPU's memory for its own pool at
+ * start-up and treats any further allocation as a failure, or a per-frame
+ * real-time pipeline that cannot risk an allocation's latency or an
+ * out-of-memory error in the middle of a frame.  This entry point does the
+ * same work (NCHW -> NHWC repack, convolution, NHWC -> NCHW repack) and calls
+ * no cudaMalloc, cudaMallocAsync, cudaFree or other allocating routine.
+ *
+ * Its scratch is one array of SC_NOALLOC_SCRATCH_FLOATS floats in the
+ * library's own device memory, present on every device that loads the
+ * library until the process exits.  A call needs
+ *   (Cin > 1 ? round_up(N*H*W*Cin, 64) : 0) + (Cout > 1 ? N*H*W*Cout : 0)
+ * floats of it; a larger problem returns SC_ERR_SHAPE before any work.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current: make that first call
+ * before any stream capture starts.  All calls share the one array and
+ * nothing is cleared between calls (every scratch element a call reads it
+ * has written first), so calls whose GPU work overlaps in time (different
+ * streams, or different host threads on one device) race on it and must be
+ * ordered by the caller.
+ * Arguments, layout (x and y NCHW), supported shapes and status codes are
+ * those of conv2d_fwd (a failed CUDA call returns SC_ERR_CUDA; its error
+ * code is not recorded for sc_last_cuda_error).
+ */
+int conv2d_fwd_nchw_noalloc(const float *x, const float *w, const float *b, float *y,
+                            int N, int H, int W, int Cin, int Cout, int R, int S,
+                            int act, sc_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

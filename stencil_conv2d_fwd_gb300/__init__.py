@@ -43,7 +43,9 @@ SIGNATURES = {
     "sc_last_cuda_error": (_I, []),
     "sc_measure_ffma_peak": (_I, [_P, _I, _I, _P]),
     "sc_version": (_I, []),
+    "conv2d_fwd_nchw_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
 }
+SC_NOALLOC_SCRATCH_FLOATS = 8 * 1024 * 1024
 
 _lib = None
 
@@ -128,6 +130,12 @@ def sc_measure_ffma_peak(sink, blocks, iters, stream=None) -> int:
 
 def sc_version() -> int:
     return load().sc_version()
+
+
+def conv2d_fwd_nchw_noalloc(x, w, b, y, N, H, W, Cin, Cout, R, S, act=SC_ACT_NONE, stream=None) -> int:
+    """NCHW conv2d_fwd that allocates no device memory (see the header)."""
+    return load().conv2d_fwd_nchw_noalloc(_ptr(x), _ptr(w), _ptr(b), _ptr(y), N, H, W, Cin, Cout, R, S,
+                                          act, _stream(stream))
 
 
 def check(status: int, what: str = "") -> None:
