@@ -39,6 +39,12 @@ L2_FLUSH_BYTES = 256 << 20
 FP32_LANES_PER_SM = 128          # FP32 FMA lanes per Blackwell SM (4 schedulers x 32)
 
 
+# --only cases: (workload id, layer index; None = the stencil pipeline)
+ONLY_CASES = {
+    "1": (1, 0), "2": (2, 0), "3-L1": (3, 0), "3-L2": (3, 1), "3-L3": (3, 2), "4": (4, 0), "5": (5, None),
+}
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -47,6 +53,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--no-per-config", action="store_true", help="skip the five-workload breakdown")
+    ap.add_argument("--only", choices=sorted(ONLY_CASES),
+                    help="launch one workload's kernel warmup+steps times and exit (for ncu captures)")
     return ap.parse_args()
 
 
@@ -521,9 +529,48 @@ def run_reference(args, rank, world):
     }))
 
 
+def run_only(args, local):
+    """One workload's kernel, launched warmup + steps times on real inputs
+    (the layer's input is the previous layer's output), for profilers."""
+    import numpy as np
+    import torch
+
+    import synthetic as S
+    import stencil_conv2d_fwd_gb300 as sc
+
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    sc.load()
+    cid, li = ONLY_CASES[args.only]
+    wl = S.config(cid)
+    if li is None:
+        ind = torch.from_numpy(wl.img).to(dev)
+        outd = torch.empty_like(ind)
+        launch = lambda: sc.stencil_pipeline_fwd(ind, outd, wl.h, wl.w)
+    else:
+        N, H, W = wl.n, wl.h, wl.w
+        x = torch.from_numpy(np.ascontiguousarray(wl.x.transpose(0, 2, 3, 1))).to(dev)
+        for k in range(li + 1):   # earlier layers produce this layer's input
+            L = wl.layers[k]
+            wd, bd = torch.from_numpy(L.w).to(dev), torch.from_numpy(L.b).to(dev)
+            y = torch.empty(N * H * W * L.cout, device=dev)
+            if k < li:
+                sc.check(sc.conv2d_fwd(x, wd, bd, y, N, H, W, L.cin, L.cout, L.r, L.s, sc.SC_NHWC, L.act))
+                x = y
+        launch = lambda: sc.conv2d_fwd(x, wd, bd, y, N, H, W, L.cin, L.cout, L.r, L.s, sc.SC_NHWC, L.act)
+    for _ in range(args.warmup + args.steps):
+        sc.check(launch())
+    torch.cuda.synchronize()
+    sc.check(sc.sc_last_device_status())
+    print(f"only {args.only}: {args.warmup + args.steps} launches ok")
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
+    if args.only:
+        run_only(args, local)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
