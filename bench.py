@@ -81,6 +81,15 @@ def kernel_source_hash(files):
     return h.hexdigest()[:16]
 
 
+def kernel_sources(L):
+    """Source files that define the kernel a conv layer runs on (for the
+    profile-staleness hash)."""
+    c = "stencil_conv2d_fwd_gb300/csrc/"
+    if L.cin == 1:
+        return [c + "conv_c1.cu", c + "common.cuh"]
+    return [c + "conv_general.cuh", c + "common.cuh", c + f"conv_general_k{max(L.r, L.s)}.cu"]
+
+
 def profiled_traffic(kernel_key: str, src_hash: str):
     """DRAM bytes per launch recorded from an ncu capture under profiles/, or
     None when absent or taken on different kernel sources."""
@@ -254,11 +263,8 @@ def run_ours(args, rank, world, local):
     Ld = layers[dom]
     dom_bytes = 4 * (N * H * W * (Ld.cin + Ld.cout) + Ld.w.size + Ld.b.size)
     achieved_tflops = flops_layer[dom] / (means[dom] * 1e-3) / 1e12
-    src_files = ["stencil_conv2d_fwd_gb300/csrc/conv_general.cuh", "stencil_conv2d_fwd_gb300/csrc/common.cuh",
-                 "stencil_conv2d_fwd_gb300/csrc/conv_general_s3.cu"] if Ld.cin > 1 else \
-                ["stencil_conv2d_fwd_gb300/csrc/conv_c1.cu", "stencil_conv2d_fwd_gb300/csrc/common.cuh"]
     key = f"conv_{Ld.cin}x{Ld.cout}_{Ld.r}x{Ld.s}_{W}x{H}"
-    traffic = profiled_traffic(key, kernel_source_hash(src_files))
+    traffic = profiled_traffic(key, kernel_source_hash(kernel_sources(Ld)))
     roofline = {
         "kernel": f"conv2d_fwd layer {dom + 1} ({Ld.cin}->{Ld.cout}, {Ld.r}x{Ld.s}, {W}x{H})",
         "bound": "alu",

@@ -122,6 +122,20 @@ int sc_measure_ffma_peak(float *sink, int blocks, int iters, sc_stream_t stream)
 /* sc_version: library version as 10000*major + 100*minor + patch. */
 int sc_version(void);
 
+/*
+ * sc_test_stencil_wait_expiry: test hook for the device-status path, not
+ * part of the operation.  Runs stencil_pipeline_fwd's TMA kernel with the
+ * copy of row chunk `drop_copy` (0-based, per warp) never issued, so each
+ * warp's time-bounded wait for it expires after `timeout_us` microseconds.
+ * The kernel then records SC_ERR_DEVICE_TIMEOUT (read and cleared by
+ * sc_last_device_status), waits for its other copies and returns; the
+ * context stays usable.  `out` is left partly written.  Needs the TMA path's
+ * conditions (W % 4 == 0, W >= 136, H >= 4, 16-byte aligned in and out),
+ * else returns SC_ERR_UNSUPPORTED.
+ */
+int sc_test_stencil_wait_expiry(const float *in, float *out, int H, int W, int drop_copy,
+                                int timeout_us, sc_stream_t stream);
+
 /* Floats of device scratch behind conv2d_fwd_nchw_noalloc (32 MiB). */
 #define SC_NOALLOC_SCRATCH_FLOATS (8u * 1024u * 1024u)
 

@@ -45,26 +45,40 @@ long long checked_count(std::initializer_list<int> dims)
     return n;
 }
 
-int launch_conv_nhwc(const sc::ConvArgs &a, cudaStream_t st)
+int conv_nhwc_status(const sc::ConvArgs &a, cudaStream_t st)
 {
-    cudaError_t e;
-    if (a.Cin == 1) {
-        e = sc::launch_conv_c1(a, st);
-    } else {
-        switch (a.S) {
-        case 1: e = sc::launch_conv_general_s1(a, st); break;
-        case 3: e = sc::launch_conv_general_s3(a, st); break;
-        case 5: e = sc::launch_conv_general_s5(a, st); break;
-        case 7: e = sc::launch_conv_general_s7(a, st); break;
-        default: return SC_ERR_UNSUPPORTED;
-        }
-    }
+    const cudaError_t e = sc::launch_conv_nhwc(a, st);
     return e == cudaSuccess ? SC_OK : cuda_fail(e);
 }
 
 }  // namespace
 
 namespace sc {
+
+cudaError_t launch_conv_nhwc(const ConvArgs &a, cudaStream_t st)
+{
+    if (a.Cin == 1) return launch_conv_c1(a, st);
+    switch (a.R > a.S ? a.R : a.S) {
+    case 1: return launch_conv_general_k1(a, st);
+    case 3: return launch_conv_general_k3(a, st);
+    case 5: return launch_conv_general_k5(a, st);
+    case 7: return launch_conv_general_k7(a, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+int *device_status_ptr()
+{
+    static int *addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+        addr[dev] = static_cast<int *>(p);
+    }
+    return addr[dev];
+}
 
 int device_sm_count()
 {
@@ -112,7 +126,7 @@ int conv2d_fwd(const float *x, const float *w, const float *b, float *y, int N, 
     sc::ConvArgs a{x, w, b, y, N, H, W, Cin, Cout, R, S, act};
     const bool need_in = (layout == SC_NCHW) && Cin > 1;
     const bool need_out = (layout == SC_NCHW) && Cout > 1;
-    if (!need_in && !need_out) return launch_conv_nhwc(a, st);
+    if (!need_in && !need_out) return conv_nhwc_status(a, st);
 
     // NCHW with channels: repack to NHWC in a stream-ordered temporary buffer.
     const size_t in_bytes = need_in ? (size_t)nx * sizeof(float) : 0;
@@ -131,7 +145,7 @@ int conv2d_fwd(const float *x, const float *w, const float *b, float *y, int N, 
     }
     if (rc == SC_OK) {
         a.y = y_nhwc;
-        rc = launch_conv_nhwc(a, st);
+        rc = conv_nhwc_status(a, st);
     }
     if (rc == SC_OK && need_out) {
         e = sc::launch_transpose_batched(y_nhwc, y, N, (long long)H * W, Cout, st);
@@ -214,5 +228,18 @@ int sc_measure_ffma_peak(float *sink, int blocks, int iters, sc_stream_t stream)
 }
 
 int sc_version(void) { return 100; }
+
+int sc_test_stencil_wait_expiry(const float *in, float *out, int H, int W, int drop_copy, int timeout_us,
+                                sc_stream_t stream)
+{
+    if (!in || !out) return SC_ERR_NULL;
+    const long long n = checked_count({H, W});
+    if (n < 0 || drop_copy < 0 || timeout_us < 1) return SC_ERR_SHAPE;
+    if (overlaps(in, (size_t)n * sizeof(float), out, (size_t)n * sizeof(float))) return SC_ERR_ALIAS;
+    const cudaError_t e = sc::launch_stencil_pipeline(in, out, H, W, reinterpret_cast<cudaStream_t>(stream),
+                                                      drop_copy, 1000ull * (unsigned long long)timeout_us);
+    if (e == cudaErrorNotSupported) return SC_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? SC_OK : cuda_fail(e);
+}
 
 }  // extern "C"

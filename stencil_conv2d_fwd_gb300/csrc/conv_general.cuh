@@ -2,35 +2,43 @@
 //
 // Method: "Optimizing Memory Efficiency for Convolution Kernels on Kepler
 // GPUs", Section 3.3 (general case) and Algorithm 2:
-//  * a CTA owns F_TB output channels ("filters") of one TH x TW block of
-//    output pixels (the 2-D TB layout, Section 3.3.1);
-//  * C_SH input channels of the block plus its halo, and the matching
-//    filter slice, are staged in shared memory per step (Fig. 6), with the
-//    next step's copy in flight while the current one is consumed
-//    (Algorithm 2's prefetch, here as cp.async double buffering);
+//  * a CTA owns F_TB output channels ("filters") and walks over TH x TW
+//    blocks of output pixels (the 2-D TB layout, Section 3.3.1);
+//  * C_SH input channels of a block plus its halo are staged in shared
+//    memory per step (Fig. 6), with the next step's copy in flight while the
+//    current one is consumed (Algorithm 2's prefetch, here cp.async double
+//    buffering that runs on across block boundaries);
 //  * each thread accumulates F_T filters x W_T horizontally contiguous
-//    pixels in registers; for one input row it keeps W_T + S - 1 pixels in
-//    registers and reuses them over the S taps of that row (Section 3.3.2);
+//    pixels in registers; for one input row it keeps W_T + K - 1 pixels in
+//    registers and reuses them over the K taps of that row (Section 3.3.2);
 //  * filter values are read as 16-byte units of 4 output channels and
 //    pixels as 16-byte units of 4 input channels, so the shared-memory access
-//    width matches the bank width (Section 2.1, W_CD = W_SMB) and a single
-//    LDS.128 feeds 4 x W_T FMAs;
-//  * pixels are read by the lanes of one warp that own different pixels,
-//    filters by the lanes that own different output channels; lanes that
-//    share a pixel (or a filter unit) read the same address (broadcast,
-//    Section 3.3.2).
+//    width matches the bank width (Section 2.1, W_CD = W_SMB) and one LDS.128
+//    feeds 4 x W_T FMAs;
+//  * lanes of a warp that own different pixels read different pixel units,
+//    lanes that own different filters read different filter units, and lanes
+//    sharing either read the same address (broadcast, Section 3.3.2).
 // Activations use the packed 4-channel layout of "Optimizing convolution
-// kernels - CNNs in Vulkan Part 2/3", section "Vectorization" (channels of
-// a pixel contiguous), so every global->shared copy is one 16-byte cp.async.
+// kernels - CNNs in Vulkan Part 2/3", section "Vectorization", so each
+// global->shared copy is one 16-byte cp.async with zero fill at the border.
 //
-// Shared-memory activation tile, per stage: [C_SH/4][TH+R-1][TWP] chunks of
-// float4, TWP = TW + S - 1, linear chunk index q, stored at chunk swz16(q, 3)
-// (XOR swizzle over 128-byte rows, "CUDA共有メモリのスウィズリング").  The
-// lanes of a warp read chunks W_T apart in one tile row; without the XOR they
-// would all fall into the same four banks.
-// Filter tile, per stage: [C_SH][R][S][F_TB] floats (filters transposed so a
-// thread's 4 output channels are one 16-byte unit).  It is written by lanes
-// that run along output channels, which is conflict-free without padding.
+// GB300 changes to the method:
+//  * Persistent CTAs: the grid is sized to the resident CTAs, and each CTA
+//    keeps its whole filter bank (all input channels, transposed to
+//    [ci][r][s][F_TB]) in shared memory for all the blocks it computes, when
+//    it fits (RESIDENT); otherwise the filter slice is staged per step.
+//  * The kernel size is a template parameter K (square); an R x S filter
+//    with R, S <= K sits centred in the K x K taps with zeros around it.
+//
+// Shared-memory activation tile per stage: [C_SH/4][TH+K-1][TWP] chunks of
+// 16 bytes, TWP = TW + K - 1 rounded up to a multiple of 8.  The pixel lanes
+// of a warp read chunks W_T apart in one tile row.  For even W_T, chunk
+// `col` of a tile row is stored at column phys_col(col): inside each group of
+// 8 chunks (128 bytes) the chunk index is XORed with the group index, the
+// swizzle of "CUDA共有メモリのスウィズリング" with 128-byte swizzle rows, which
+// puts those lanes in different bank groups with a constant key per lane.
+// For odd W_T the plain layout is already conflict-free (and the XOR would
+// not be).
 #pragma once
 
 #include "common.cuh"
@@ -38,15 +46,19 @@
 
 namespace sc {
 
-template <int S_, int F_TB_, int W_T_, int TH_, int TW_, int C_SH_, int MINB_>
+template <int K_, int F_TB_, int W_T_, int TH_, int TW_, int C_SH_, bool RESIDENT_, int MINB_>
 struct GenCfg {
-    static constexpr int S = S_;
+    static constexpr int K = K_;
     static constexpr int F_TB = F_TB_;
     static constexpr int W_T = W_T_;
     static constexpr int TH = TH_;
     static constexpr int TW = TW_;
     static constexpr int C_SH = C_SH_;
-    static constexpr int MINB = MINB_;
+    static constexpr bool RESIDENT = RESIDENT_;
+    static constexpr int MINB = MINB_;                   // CTAs per SM the registers must allow
+    // Pixel lanes read chunks W_T apart.  An odd stride already spreads 8
+    // lanes over 8 bank groups; an even one needs the XOR swizzle.
+    static constexpr bool SWZ = (W_T % 2) == 0;
     static constexpr int F_T = F_TB >= 8 ? 8 : 4;       // output channels per thread
     static constexpr int NG = F_T / 4;                   // float4 groups per thread
     static constexpr int T_X = F_TB / F_T;               // lanes along output channels
@@ -56,173 +68,227 @@ struct GenCfg {
     static constexpr int NWARPS = WARPS_PER_ROW * TH;
     static constexpr int NT = NWARPS * 32;
     static constexpr int CB = C_SH / 4;
-    static constexpr int TWP = TW + S - 1;
-    static constexpr int WIN = W_T + S - 1;
+    static constexpr int KK = K * K;
+    static constexpr int THh = TH + K - 1;
+    static constexpr int TWU = TW + K - 1;               // tile row width used
+    static constexpr int TWP = (TWU + 7) & ~7;           // tile row pitch (chunks)
+    static constexpr int WIN = W_T + K - 1;
+    static constexpr int IN_CHUNKS = CB * THh * TWP;     // multiple of 8
+    static constexpr int STAGE_W = RESIDENT ? 0 : C_SH * KK * F_TB;
+    static constexpr int STAGE_FLOATS = IN_CHUNKS * 4 + STAGE_W;
     static_assert(F_TB % F_T == 0 && 32 % T_X == 0, "bad channel split");
     static_assert(TW % WARP_COLS == 0, "tile width must hold whole warps");
     static_assert(C_SH % 4 == 0, "C_SH must be a multiple of 4");
     static_assert(NT <= 1024, "too many threads");
 
-    // Activation chunks per stage for R rows of taps.  The swizzle permutes
-    // chunks inside rows of 8, so the tile is padded to whole rows of 8: the
-    // physical index of logical chunk q < used_chunks stays below this.
-    static __host__ __device__ int used_chunks(int R) { return CB * (TH + R - 1) * TWP; }
-    static __host__ __device__ int in_chunks(int R) { return (used_chunks(R) + 7) & ~7; }
-    // floats per stage: activation chunks * 4 + filters
-    static __host__ __device__ int w_floats(int R) { return C_SH * R * S * F_TB; }
-    static __host__ __device__ int stage_floats(int R) { return in_chunks(R) * 4 + w_floats(R); }
-    static size_t smem_bytes(int R) { return 2 * size_t(stage_floats(R)) * sizeof(float); }
+    // shared memory: [resident filters][stage 0][stage 1]
+    static __host__ __device__ size_t w_res_floats(int cin_pad)
+    {
+        return RESIDENT ? (size_t)cin_pad * KK * F_TB : 0;
+    }
+    static size_t smem_bytes(int cin_pad) { return (w_res_floats(cin_pad) + 2 * (size_t)STAGE_FLOATS) * 4; }
 };
 
+// Physical chunk column of logical chunk column `col` in a tile row.
 template <class C>
-__device__ __forceinline__ void gen_issue_stage(float *stage, const float *__restrict__ x,
-                                                const float *__restrict__ w, int n, int y0,
-                                                int x0, int co0, int c0, int H, int W, int Cin,
-                                                int Cout, int R, int tid)
+__host__ __device__ __forceinline__ int phys_col(int col) { return C::SWZ ? swz16(col, 3) : col; }
+
+// Copy filters for input channels [c0, c0 + nci) into ws[(ci-c0)*KK + r*K + s][F_TB]
+// (transposed, output channels contiguous), zero where the R x S filter has
+// no tap, where co >= Cout or ci >= Cin.  Lanes run along output channels,
+// so the shared-memory side is contiguous.
+template <class C>
+__device__ __forceinline__ void gen_issue_filters(float *ws, const float *__restrict__ w, int co0,
+                                                  int c0, int nci, int Cin, int Cout, int R, int S,
+                                                  int tid)
 {
-    float4 *in_s = reinterpret_cast<float4 *>(stage);
-    float *w_s = stage + C::in_chunks(R) * 4;
-    const int THh = C::TH + R - 1;
-    const int nq = C::used_chunks(R);
-    // activation halo tile: one 16-byte chunk (4 channels of a pixel) per copy
-    for (int q = tid; q < nq; q += C::NT) {
-        const int xx = q % C::TWP;
-        const int t = q / C::TWP;
-        const int yy = t % THh;
-        const int cb = t / THh;
-        const int gy = y0 - R / 2 + yy;
-        const int gx = x0 - C::S / 2 + xx;
-        const int ci = c0 + 4 * cb;
-        const bool ok = (gy >= 0) & (gy < H) & (gx >= 0) & (gx < W) & (ci < Cin);
-        const float *src = ok ? x + ((((long long)n * H + gy) * W + gx) * Cin + ci) : x;
-        cp_async16(smem_u32(in_s + swz16(q, 3)), src, ok ? 16 : 0);
-    }
-    // filter slice [C_SH][R][S][F_TB], lanes along output channels
-    const int RS = R * C::S;
-    const int nw = C::C_SH * RS * C::F_TB;
-    for (int e = tid; e < nw; e += C::NT) {
+    const int n = nci * C::KK * C::F_TB;
+    const int dr = (C::K - R) / 2, ds = (C::K - S) / 2;
+    for (int e = tid; e < n; e += C::NT) {
         const int col = e % C::F_TB;
-        const int row = e / C::F_TB;  // = ci_l * RS + rs
-        const int ci = c0 + row / RS;
-        const int rs = row % RS;
+        const int row = e / C::F_TB;
+        const int ci = c0 + row / C::KK;
+        const int rs = row % C::KK;
+        const int r = rs / C::K - dr;
+        const int s = rs % C::K - ds;
         const int co = co0 + col;
-        const bool ok = (co < Cout) & (ci < Cin);
-        const float *src = ok ? w + (((long long)co * Cin + ci) * RS + rs) : w;
-        cp_async4(smem_u32(w_s + e), src, ok ? 4 : 0);
+        const bool ok = (co < Cout) & (ci < Cin) & (r >= 0) & (r < R) & (s >= 0) & (s < S);
+        const float *src = ok ? w + ((((long long)co * Cin + ci) * R + r) * S + s) : w;
+        cp_async4(smem_u32(ws + e), src, ok ? 4 : 0);
+    }
+}
+
+// Activation halo tile of output block (n, y0, x0), input channels
+// [c0, c0 + C_SH): one 16-byte cp.async per (channel block, row, column),
+// zero-filled outside the image and beyond Cin.  Each warp copies whole
+// tile rows, its lanes along the row, so the per-copy index arithmetic is a
+// few adds; 32 consecutive columns of a row never share a bank group.
+template <class C>
+__device__ __forceinline__ void gen_issue_tile(float4 *in_s, const float *__restrict__ x, int n, int y0,
+                                               int x0, int c0, int H, int W, int Cin, int warp, int lane)
+{
+    for (int rowi = warp; rowi < C::CB * C::THh; rowi += C::NWARPS) {
+        const int cb = rowi / C::THh;
+        const int yy = rowi % C::THh;
+        const int gy = y0 - C::K / 2 + yy;
+        const int ci = c0 + 4 * cb;
+        const bool row_ok = (gy >= 0) & (gy < H) & (ci < Cin);
+        const float *grow = x + ((((long long)n * H + (row_ok ? gy : 0)) * W) * Cin + (row_ok ? ci : 0));
+        float4 *srow = in_s + rowi * C::TWP;
+        for (int xx = lane; xx < C::TWU; xx += 32) {
+            const int gx = x0 - C::K / 2 + xx;
+            const bool ok = row_ok & (gx >= 0) & (gx < W);
+            const float *src = ok ? grow + (long long)gx * Cin : x;
+            cp_async16(smem_u32(srow + phys_col<C>(xx)), src, ok ? 16 : 0);
+        }
     }
 }
 
 template <class C>
 __global__ void __launch_bounds__(C::NT, C::MINB)
     conv_general_kernel(const float *__restrict__ x, const float *__restrict__ w,
-                        const float *__restrict__ bias, float *__restrict__ y, int N, int H,
-                        int W, int Cin, int Cout, int R, int act, int tiles_x, int tiles_y)
+                        const float *__restrict__ bias, float *__restrict__ y, int N, int H, int W,
+                        int Cin, int Cout, int R, int S, int act, int tiles_x, int tiles_y)
 {
-    extern __shared__ __align__(16) float smem[];
+    extern __shared__ __align__(128) float smem[];
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int tx = lane % C::T_X;        // output-channel lane
     const int pl = lane / C::T_X;        // pixel lane
-
-    int tile = blockIdx.x;
-    const int txi = tile % tiles_x;
-    tile /= tiles_x;
-    const int tyi = tile % tiles_y;
-    const int n = tile / tiles_y;
     const int co0 = blockIdx.y * C::F_TB;
-    const int y0 = tyi * C::TH;
-    const int x0 = txi * C::TW;
-
     const int ry = warp / C::WARPS_PER_ROW;                                   // tile row
     const int cx0 = (warp % C::WARPS_PER_ROW) * C::WARP_COLS + pl * C::W_T;   // tile col
 
-    const int stage_f = C::stage_floats(R);
-    const int THh = C::TH + R - 1;
-    const int nk = (Cin + C::C_SH - 1) / C::C_SH;
+    const int cin_pad = (Cin + C::C_SH - 1) / C::C_SH * C::C_SH;
+    const int nk = cin_pad / C::C_SH;
+    const int ntiles = tiles_x * tiles_y * N;
+    float *w_res = smem;
+    float *stage0 = smem + C::w_res_floats(cin_pad);
 
-    float acc[C::F_T][C::W_T];
+    // pixel-column offsets of this lane's row window (constant over the run)
+    int pcol[C::WIN];
 #pragma unroll
-    for (int f = 0; f < C::F_T; ++f)
-#pragma unroll
-        for (int j = 0; j < C::W_T; ++j) acc[f][j] = 0.0f;
+    for (int j = 0; j < C::WIN; ++j) pcol[j] = phys_col<C>(cx0 + j);
 
-    gen_issue_stage<C>(smem, x, w, n, y0, x0, co0, 0, H, W, Cin, Cout, R, tid);
+    float bv[C::F_T];
+#pragma unroll
+    for (int g = 0; g < C::NG; ++g)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int co = co0 + g * (C::F_TB / C::NG) + 4 * tx + e;
+            bv[4 * g + e] = (bias && co < Cout) ? bias[co] : 0.0f;
+        }
+
+    int tile = blockIdx.x;
+    if (tile >= ntiles) return;
+    auto decode = [&](int t, int &n, int &y0, int &x0) {
+        x0 = (t % tiles_x) * C::TW;
+        t /= tiles_x;
+        y0 = (t % tiles_y) * C::TH;
+        n = t / tiles_y;
+    };
+    auto issue = [&](int t, int k, int buf) {
+        int n, y0, x0;
+        decode(t, n, y0, x0);
+        float *st = stage0 + buf * C::STAGE_FLOATS;
+        gen_issue_tile<C>(reinterpret_cast<float4 *>(st), x, n, y0, x0, k * C::C_SH, H, W, Cin, warp, lane);
+        if constexpr (!C::RESIDENT)
+            gen_issue_filters<C>(st + C::IN_CHUNKS * 4, w, co0, k * C::C_SH, C::C_SH, Cin, Cout, R, S, tid);
+    };
+
+    if constexpr (C::RESIDENT) gen_issue_filters<C>(w_res, w, co0, 0, cin_pad, Cin, Cout, R, S, tid);
+    issue(tile, 0, 0);
     cp_async_commit();
 
-    for (int k = 0; k < nk; ++k) {
-        if (k + 1 < nk) {
-            gen_issue_stage<C>(smem + ((k + 1) & 1) * stage_f, x, w, n, y0, x0, co0,
-                               (k + 1) * C::C_SH, H, W, Cin, Cout, R, tid);
-            cp_async_commit();
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncthreads();
+    int it = 0;
+    for (; tile < ntiles; tile += gridDim.x) {
+        float acc[C::F_T][C::W_T];
+#pragma unroll
+        for (int f = 0; f < C::F_T; ++f)
+#pragma unroll
+            for (int j = 0; j < C::W_T; ++j) acc[f][j] = 0.0f;
 
-        const float *stage = smem + (k & 1) * stage_f;
-        const float4 *in_s = reinterpret_cast<const float4 *>(stage);
-        const float4 *w_s4 = reinterpret_cast<const float4 *>(stage + C::in_chunks(R) * 4);
+        for (int k = 0; k < nk; ++k, ++it) {
+            // prefetch the next step: the next channel chunk, or the first
+            // chunk of this CTA's next block
+            const int nt = (k + 1 < nk) ? tile : tile + (int)gridDim.x;
+            const int nkk = (k + 1 < nk) ? k + 1 : 0;
+            if (nt < ntiles) {
+                issue(nt, nkk, (it + 1) & 1);
+                cp_async_commit();
+                cp_async_wait<1>();
+            } else {
+                cp_async_wait<0>();
+            }
+            __syncthreads();
 
+            const float *st = stage0 + (it & 1) * C::STAGE_FLOATS;
+            const float4 *in_s = reinterpret_cast<const float4 *>(st);
+            const float4 *w_s4 =
+                C::RESIDENT ? reinterpret_cast<const float4 *>(w_res) + (size_t)k * C::C_SH * C::KK * (C::F_TB / 4)
+                            : reinterpret_cast<const float4 *>(st + C::IN_CHUNKS * 4);
 #pragma unroll 1
-        for (int cb = 0; cb < C::CB; ++cb) {
+            for (int cb = 0; cb < C::CB; ++cb) {
 #pragma unroll 1
-            for (int r = 0; r < R; ++r) {
-                // one input row of W_T + S - 1 pixels x 4 channels
-                const int base = (cb * THh + ry + r) * C::TWP + cx0;
-                float4 px[C::WIN];
+                for (int r = 0; r < C::K; ++r) {
+                    // one input row: W_T + K - 1 pixels x 4 channels
+                    const float4 *row = in_s + (cb * C::THh + ry + r) * C::TWP;
+                    float4 px[C::WIN];
 #pragma unroll
-                for (int j = 0; j < C::WIN; ++j) px[j] = in_s[swz16(base + j, 3)];
-                // filter rows of (ci = 4cb + c, r, s): ((4cb + c) * R + r) * S + s
-                const float4 *wr = w_s4 + ((4 * cb * R + r) * C::S) * (C::F_TB / 4) + tx;
+                    for (int j = 0; j < C::WIN; ++j) px[j] = row[pcol[j]];
+                    // filter rows ((4cb + c) * K + r) * K + s
+                    const float4 *wr = w_s4 + (4 * cb * C::KK + r * C::K) * (C::F_TB / 4) + tx;
 #pragma unroll
-                for (int s = 0; s < C::S; ++s) {
+                    for (int s = 0; s < C::K; ++s) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const float4 *wp = wr + (c * R * C::S + s) * (C::F_TB / 4);
-                        float wv[C::F_T];
+                        for (int c = 0; c < 4; ++c) {
+                            const float4 *wp = wr + (c * C::KK + s) * (C::F_TB / 4);
+                            float wv[C::F_T];
 #pragma unroll
-                        for (int g = 0; g < C::NG; ++g) {
-                            const float4 t = wp[g * C::T_X];
-                            wv[4 * g + 0] = t.x;
-                            wv[4 * g + 1] = t.y;
-                            wv[4 * g + 2] = t.z;
-                            wv[4 * g + 3] = t.w;
-                        }
+                            for (int g = 0; g < C::NG; ++g) {
+                                const float4 t = wp[g * C::T_X];
+                                wv[4 * g + 0] = t.x;
+                                wv[4 * g + 1] = t.y;
+                                wv[4 * g + 2] = t.z;
+                                wv[4 * g + 3] = t.w;
+                            }
 #pragma unroll
-                        for (int j = 0; j < C::W_T; ++j) {
-                            const float4 p = px[j + s];
-                            const float v = c == 0 ? p.x : (c == 1 ? p.y : (c == 2 ? p.z : p.w));
+                            for (int j = 0; j < C::W_T; ++j) {
+                                const float4 p = px[j + s];
+                                const float v = c == 0 ? p.x : (c == 1 ? p.y : (c == 2 ? p.z : p.w));
 #pragma unroll
-                            for (int f = 0; f < C::F_T; ++f) acc[f][j] = fmaf(wv[f], v, acc[f][j]);
+                                for (int f = 0; f < C::F_T; ++f) acc[f][j] = fmaf(wv[f], v, acc[f][j]);
+                            }
                         }
                     }
                 }
             }
+            __syncthreads();
         }
-        __syncthreads();
-    }
 
-    // epilogue: bias, activation, 16-byte NHWC stores of 4 output channels
-    const int gy = y0 + ry;
-    if (gy >= H) return;
+        // epilogue: bias, activation, 16-byte NHWC stores of 4 output channels
+        int n, y0, x0;
+        decode(tile, n, y0, x0);
+        const int gy = y0 + ry;
+        if (gy < H) {
 #pragma unroll
-    for (int g = 0; g < C::NG; ++g) {
-        const int co = co0 + g * (C::F_TB / C::NG) + 4 * tx;
-        if (co >= Cout) continue;
-        float4 bv = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (bias) bv = make_float4(bias[co], bias[co + 1], bias[co + 2], bias[co + 3]);
+            for (int g = 0; g < C::NG; ++g) {
+                const int co = co0 + g * (C::F_TB / C::NG) + 4 * tx;
+                if (co < Cout) {
 #pragma unroll
-        for (int j = 0; j < C::W_T; ++j) {
-            const int gx = x0 + cx0 + j;
-            if (gx < W) {
-                float4 o;
-                o.x = relu_if(acc[4 * g + 0][j] + bv.x, act);
-                o.y = relu_if(acc[4 * g + 1][j] + bv.y, act);
-                o.z = relu_if(acc[4 * g + 2][j] + bv.z, act);
-                o.w = relu_if(acc[4 * g + 3][j] + bv.w, act);
-                *reinterpret_cast<float4 *>(y + ((((long long)n * H + gy) * W + gx) * Cout + co)) = o;
+                    for (int j = 0; j < C::W_T; ++j) {
+                        const int gx = x0 + cx0 + j;
+                        if (gx < W) {
+                            float4 o;
+                            o.x = relu_if(acc[4 * g + 0][j] + bv[4 * g + 0], act);
+                            o.y = relu_if(acc[4 * g + 1][j] + bv[4 * g + 1], act);
+                            o.z = relu_if(acc[4 * g + 2][j] + bv[4 * g + 2], act);
+                            o.w = relu_if(acc[4 * g + 3][j] + bv[4 * g + 3], act);
+                            *reinterpret_cast<float4 *>(y + ((((long long)n * H + gy) * W + gx) * Cout + co)) = o;
+                        }
+                    }
+                }
             }
         }
     }
@@ -236,36 +302,75 @@ cudaError_t launch_gen(const ConvArgs &a, cudaStream_t st)
     const long long nt = (long long)tiles_x * tiles_y * a.N;
     const int groups = (a.Cout + C::F_TB - 1) / C::F_TB;
     if (nt > 0x7fffffffLL || groups > 65535) return cudaErrorInvalidConfiguration;
-    const size_t smem = C::smem_bytes(a.R);
-    if (smem > 48 * 1024) {
-        // opt in to more than 48 KB once per device (largest size seen so far)
-        static int allowed[64] = {0};
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
+    const int cin_pad = (a.Cin + C::C_SH - 1) / C::C_SH * C::C_SH;
+    const size_t smem = C::smem_bytes(cin_pad);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    // per device: the largest dynamic shared memory opted in so far, and the
+    // resident CTAs per SM at the last size queried
+    static int allowed[64] = {0};
+    static int per_sm[64] = {0};
+    static int per_sm_smem[64] = {0};
+    if (smem > 48 * 1024 && allowed[dev] < (int)smem) {
+        e = cudaFuncSetAttribute(conv_general_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        if (dev < 0 || dev >= 64 || allowed[dev] < (int)smem) {
-            e = cudaFuncSetAttribute(conv_general_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem);
-            if (e != cudaSuccess) return e;
-            if (dev >= 0 && dev < 64) allowed[dev] = (int)smem;
-        }
+        allowed[dev] = (int)smem;
     }
-    conv_general_kernel<C><<<dim3((unsigned)nt, groups), C::NT, smem, st>>>(
-        a.x, a.w, a.b, a.y, a.N, a.H, a.W, a.Cin, a.Cout, a.R, a.act, tiles_x, tiles_y);
+    if (per_sm_smem[dev] != (int)smem) {
+        int b = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, conv_general_kernel<C>, C::NT, smem);
+        if (e != cudaSuccess) return e;
+        per_sm[dev] = b > 0 ? b : 1;
+        per_sm_smem[dev] = (int)smem;
+    }
+    // persistent grid: the resident CTAs, shared out among the output-channel groups
+    const long long slots = (long long)per_sm[dev] * device_sm_count();
+    long long gx = (slots + groups - 1) / groups;
+    if (gx > nt) gx = nt;
+    if (gx < 1) gx = 1;
+    conv_general_kernel<C><<<dim3((unsigned)gx, groups), C::NT, smem, st>>>(
+        a.x, a.w, a.b, a.y, a.N, a.H, a.W, a.Cin, a.Cout, a.R, a.S, a.act, tiles_x, tiles_y);
     return cudaGetLastError();
 }
 
-// Tile table.  Chosen per output-channel count; the width of a warp's pixel
-// run (PXL * W_T) and the tile height set how many CTAs a layer gets.
-template <int S>
+// Filters of one output-channel group stay resident in shared memory when
+// they take at most this much.
+constexpr size_t kResidentFilterBytes = 160 * 1024;
+
+template <int K, int F_TB, int W_T, int TH, int TW, int C_SH, int MINB>
+cudaError_t launch_gen_auto(const ConvArgs &a, cudaStream_t st)
+{
+    const size_t cin_pad = (size_t)(a.Cin + C_SH - 1) / C_SH * C_SH;
+    if (cin_pad * K * K * F_TB * 4 <= kResidentFilterBytes)
+        return launch_gen<GenCfg<K, F_TB, W_T, TH, TW, C_SH, true, MINB>>(a, st);
+    return launch_gen<GenCfg<K, F_TB, W_T, TH, TW, C_SH, false, MINB>>(a, st);
+}
+
+// Columns computed beyond the image edge when rows are cut into tiles of tw.
+inline int tile_waste(int W, int tw) { return (W + tw - 1) / tw * tw - W; }
+
+// Tile table for kernel size K (measured on GB300 for 3x3 layers).  One CTA
+// per SM with 168 registers per thread beats two CTAs at 128: with fewer
+// registers the FFMA stream stalls more at dispatch.  The pixel run per
+// thread is 8 or 7, whichever wastes fewer columns at the image edge.
+template <int K>
 cudaError_t dispatch_general(const ConvArgs &a, cudaStream_t st)
 {
-    // C_SH = 8 channels per stage for all; smaller Cin is zero-padded in smem.
-    if (a.Cout > 48) return launch_gen<GenCfg<S, 64, 8, 8, 32, 8, 1>>(a, st);
-    if (a.Cout > 16) return launch_gen<GenCfg<S, 32, 8, 8, 64, 8, 1>>(a, st);
-    if (a.Cout > 8) return launch_gen<GenCfg<S, 16, 4, 4, 64, 8, 2>>(a, st);
-    if (a.Cout > 4) return launch_gen<GenCfg<S, 8, 4, 4, 128, 8, 2>>(a, st);
-    return launch_gen<GenCfg<S, 4, 8, 4, 256, 8, 2>>(a, st);
+    // 7x7 filter slices staged per step need half the channels per stage
+    constexpr int CS = K >= 7 ? 4 : 8;
+    if (a.Cout > 32) {
+        if (tile_waste(a.W, 28) < tile_waste(a.W, 32)) return launch_gen_auto<K, 64, 7, 8, 28, CS, 1>(a, st);
+        return launch_gen_auto<K, 64, 8, 8, 32, CS, 1>(a, st);
+    }
+    if (a.Cout > 16) {
+        if (tile_waste(a.W, 56) < tile_waste(a.W, 64)) return launch_gen_auto<K, 32, 7, 4, 56, CS, 1>(a, st);
+        return launch_gen_auto<K, 32, 8, 4, 64, CS, 1>(a, st);
+    }
+    if (a.Cout > 8) return launch_gen_auto<K, 16, 4, 4, 64, CS, 2>(a, st);
+    if (a.Cout > 4) return launch_gen_auto<K, 8, 4, 4, 128, CS, 2>(a, st);
+    return launch_gen_auto<K, 4, 8, 4, 256, CS, 2>(a, st);
 }
 
 }  // namespace sc

@@ -14,17 +14,25 @@ struct ConvArgs {
     int N, H, W, Cin, Cout, R, S, act;
 };
 
-// General direct convolution, Cin % 4 == 0, Cout % 4 == 0 (conv_general_s*.cu).
-cudaError_t launch_conv_general_s1(const ConvArgs &a, cudaStream_t st);
-cudaError_t launch_conv_general_s3(const ConvArgs &a, cudaStream_t st);
-cudaError_t launch_conv_general_s5(const ConvArgs &a, cudaStream_t st);
-cudaError_t launch_conv_general_s7(const ConvArgs &a, cudaStream_t st);
+// General direct convolution, Cin % 4 == 0, Cout % 4 == 0, filters up to
+// K x K (conv_general_k*.cu).
+cudaError_t launch_conv_general_k1(const ConvArgs &a, cudaStream_t st);
+cudaError_t launch_conv_general_k3(const ConvArgs &a, cudaStream_t st);
+cudaError_t launch_conv_general_k5(const ConvArgs &a, cudaStream_t st);
+cudaError_t launch_conv_general_k7(const ConvArgs &a, cudaStream_t st);
+
+// NHWC convolution: picks the single-input-channel kernel or the general
+// kernel for K = max(R, S) (api.cu).
+cudaError_t launch_conv_nhwc(const ConvArgs &a, cudaStream_t st);
 
 // Single-input-channel convolution, Cout == 1 or Cout % 4 == 0 (conv_c1.cu).
 cudaError_t launch_conv_c1(const ConvArgs &a, cudaStream_t st);
 
-// Fused blur/unsharp pipeline (stencil.cu).
-cudaError_t launch_stencil_pipeline(const float *in, float *out, int H, int W, cudaStream_t st);
+// Fused blur/unsharp pipeline (stencil.cu).  drop_copy >= 0 leaves that
+// TMA copy of every warp un-issued so its bounded wait expires (tests of the
+// device-status path); timeout_ns bounds each wait.
+cudaError_t launch_stencil_pipeline(const float *in, float *out, int H, int W, cudaStream_t st,
+                                    int drop_copy = -1, unsigned long long timeout_ns = 1000000000ull);
 
 // dst[n][b][a] = src[n][a][b] (repack.cu): NCHW->NHWC is (A=C, B=H*W),
 // NHWC->NCHW is (A=H*W, B=C).
@@ -36,5 +44,12 @@ cudaError_t launch_ffma_peak(float *sink, int blocks, int iters, cudaStream_t st
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
+
+// Device address of the current device's status word (api.cu), or nullptr.
+int *device_status_ptr();
+
+// Value kernels store in the status word when a bounded wait expires
+// (SC_ERR_DEVICE_TIMEOUT of include/stencilconv.h).
+constexpr int kDeviceTimeout = -7;
 
 }  // namespace sc

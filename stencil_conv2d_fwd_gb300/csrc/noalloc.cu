@@ -102,16 +102,7 @@ extern "C" int conv2d_fwd_nchw_noalloc(const float *x, const float *w, const flo
         a.x = scratch;
     }
     if (Cout > 1) a.y = scratch + off;
-    if (Cin == 1) {
-        e = sc::launch_conv_c1(a, st);
-    } else {
-        switch (S) {
-        case 1: e = sc::launch_conv_general_s1(a, st); break;
-        case 3: e = sc::launch_conv_general_s3(a, st); break;
-        case 5: e = sc::launch_conv_general_s5(a, st); break;
-        default: e = sc::launch_conv_general_s7(a, st); break;
-        }
-    }
+    e = sc::launch_conv_nhwc(a, st);
     if (e != cudaSuccess) return fail(e);
     if (Cout > 1) {
         e = sc::launch_transpose_batched(scratch + off, y, N, (long long)H * W, Cout, st);

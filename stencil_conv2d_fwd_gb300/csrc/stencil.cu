@@ -5,20 +5,32 @@
 // on GPUs" (Abstract): the stages are fused into tiles that fit one warp, so
 // the only synchronisation is within the warp, and the overlapped (halo)
 // part of the tile lives in thread registers rather than in block-shared
-// memory (hybrid tiling).  Here a warp owns a strip 128 columns wide (4
-// contiguous pixels per lane, one 16-byte load) and walks down a band of
-// rows:
-//  * per input row, a lane's 2 + 2 horizontal halo pixels come from its
-//    neighbour lanes' registers by shuffle; only lanes 0 and 31 load theirs;
+// memory (hybrid tiling).  A warp owns a strip 128 columns wide (4
+// contiguous pixels per lane) and walks down a band of rows:
 //  * the horizontal pass t1 of the last five rows stays in registers (a
-//    5-row ring), as do the matching input rows for the unsharp step;
-//  * the vertical pass and the unsharp mask run on the ring, and the output
-//    row leaves as one 16-byte store per lane.
-// The only recomputation is the 4-row vertical overlap at each band's
-// edges.  Nothing but `in` and `out` touches global memory.
-// Clamp-to-edge is applied to indices: a lane's pixels beyond the last
-// column read in[row][W-1], so neighbour lanes hand out clamped halos for
-// free; rows outside [0, H) read row 0 or H-1.
+//    5-row window), as do the matching input rows for the unsharp step;
+//  * the vertical pass and the unsharp mask run on the window, and each
+//    output row leaves as one 16-byte store per lane;
+//  * the only recomputation is the 4-row vertical overlap at each band's
+//    edges; nothing but `in` and `out` touches global memory.
+// Clamp-to-edge: a row outside [0, H) is the first or last row, repeated; a
+// column outside [0, W) is the first or last column.
+//
+// Two ways to bring rows in:
+//  * stencil_tma_kernel (GB300 path): each warp streams its strip through a
+//    ring of 4 shared-memory slots of 4 rows x 136 columns (its 128 columns
+//    plus 4 on each side), filled by 2-D TMA copies (cp.async.bulk.tensor)
+//    that complete on one mbarrier per slot, so three slots' copies are in
+//    flight while the fourth is consumed.  Lanes read their 4 pixels and 2 + 2
+//    halo pixels from the slot.  Waits are bounded in time; on expiry the
+//    kernel records SC_ERR_DEVICE_TIMEOUT, drains its copies and returns.
+//  * stencil_regs_kernel (any size or alignment): each lane loads its 4
+//    pixels; the halo pixels come from the neighbour lanes by shuffle.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -88,7 +100,7 @@ __device__ __forceinline__ float st_unsharp(float in, float t2)
 }
 
 __global__ void __launch_bounds__(ST_NWARPS * 32)
-    stencil_pipeline_kernel(const float *__restrict__ in, float *__restrict__ out, int H, int W,
+    stencil_regs_kernel(const float *__restrict__ in, float *__restrict__ out, int H, int W,
                             int rows_per_cta, int col_tiles, int vec)
 {
     const int lane = threadIdx.x & 31;
@@ -150,8 +162,164 @@ __global__ void __launch_bounds__(ST_NWARPS * 32)
     }
 }
 
-cudaError_t launch_stencil_pipeline(const float *in, float *out, int H, int W, cudaStream_t st)
+// ---------------------------------------------------------------------------
+// TMA path
+// ---------------------------------------------------------------------------
+static constexpr int TS_WARPS = 4;                 // warps per CTA
+static constexpr int TS_D = 4;                     // ring slots per warp
+static constexpr int TS_RB = 4;                    // rows per slot (TMA box height)
+static constexpr int TS_SW = 136;                  // columns per slot row: x0-4 .. x0+131
+static constexpr int TS_SLOT = TS_RB * TS_SW;      // floats per slot
+static constexpr unsigned TS_SLOT_BYTES = TS_SLOT * 4;
+
+// Number of times input row yy occurs in the clamped row sequence
+// clamp(v, 0, H-1), v = y0-2 .. y1+1, that a band [y0, y1) consumes.
+__device__ __forceinline__ int st_row_count(int yy, int y0, int y1, int H)
 {
+    int a = yy == 0 ? y0 - 2 : yy;
+    int b = yy == H - 1 ? y1 + 1 : yy;
+    a = max(a, y0 - 2);
+    b = min(b, y1 + 1);
+    return max(0, b - a + 1);
+}
+
+__global__ void __launch_bounds__(TS_WARPS * 32)
+    stencil_tma_kernel(const __grid_constant__ CUtensorMap tm, float *__restrict__ out, int H, int W,
+                       int band, int nstrips, int *status, unsigned long long timeout_ns, int drop_copy)
+{
+    __shared__ __align__(128) float ring[TS_WARPS][TS_D][TS_SLOT];
+    __shared__ __align__(8) unsigned long long bars[TS_WARPS][TS_D];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int gw = blockIdx.x * TS_WARPS + warp;
+    const int strip = gw % nstrips;
+    const int y0 = (gw / nstrips) * band;
+    if (y0 >= H) return;  // whole warp
+    const int y1 = min(H, y0 + band);
+    const int xs = strip * ST_COLS_PER_WARP;
+    const int ys = max(y0 - 2, 0), ye = min(y1 + 2, H);      // input rows [ys, ye)
+    const int nchunks = (ye - ys + TS_RB - 1) / TS_RB;
+    float *slots = &ring[warp][0][0];
+    const uint32_t bar0 = smem_u32(&bars[warp][0]);
+
+    if (lane == 0) {
+#pragma unroll
+        for (int d = 0; d < TS_D; ++d) mbar_init(bar0 + 8 * d, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    auto issue = [&](int c) {  // lane 0: rows ys + 4c .. ys + 4c + 3 into slot c % D
+        const int d = c % TS_D;
+        mbar_arrive_expect_tx(bar0 + 8 * d, TS_SLOT_BYTES);
+        if (c != drop_copy) tma_load_2d(smem_u32(slots + d * TS_SLOT), &tm, xs - 4, ys + c * TS_RB, bar0 + 8 * d);
+    };
+    if (lane == 0)
+        for (int c = 0; c < min(TS_D, nchunks); ++c) issue(c);
+
+    const int x0 = xs + 4 * lane;
+    float4 t[5], iv[3];
+    int nv = 0;
+    int c = 0;
+    bool failed = false;
+    for (; c < nchunks; ++c) {
+        const int d = c % TS_D;
+        if (!mbar_wait_bounded(bar0 + 8 * d, (c / TS_D) & 1, timeout_ns)) {
+            failed = true;
+            break;
+        }
+        const float *sl = slots + d * TS_SLOT;
+        for (int j = 0; j < TS_RB; ++j) {
+            const int yy = ys + c * TS_RB + j;
+            if (yy >= ye) break;
+            const float *rp = sl + j * TS_SW;
+            const float4 own = *reinterpret_cast<const float4 *>(rp + 4 + 4 * lane);
+            float2 lh = *reinterpret_cast<const float2 *>(rp + 2 + 4 * lane);
+            float2 rh = *reinterpret_cast<const float2 *>(rp + 8 + 4 * lane);
+            if (x0 == 0) lh = make_float2(own.x, own.x);          // columns -2, -1
+            if (x0 + 4 >= W) rh = make_float2(own.w, own.w);      // columns W, W+1 (W % 4 == 0)
+            Row8 r;
+            r.v[0] = lh.x; r.v[1] = lh.y; r.v[2] = own.x; r.v[3] = own.y;
+            r.v[4] = own.z; r.v[5] = own.w; r.v[6] = rh.x; r.v[7] = rh.y;
+            const float4 t1 = st_hblur(r);
+            for (int k = st_row_count(yy, y0, y1, H); k > 0; --k) {
+                t[0] = t[1]; t[1] = t[2]; t[2] = t[3]; t[3] = t[4]; t[4] = t1;
+                iv[0] = iv[1]; iv[1] = iv[2]; iv[2] = own;
+                if (++nv >= 5) {
+                    const int oy = y0 + nv - 5;
+                    float4 o;
+                    o.x = st_unsharp(iv[0].x, st_vblur1(t[0].x, t[1].x, t[2].x, t[3].x, t[4].x));
+                    o.y = st_unsharp(iv[0].y, st_vblur1(t[0].y, t[1].y, t[2].y, t[3].y, t[4].y));
+                    o.z = st_unsharp(iv[0].z, st_vblur1(t[0].z, t[1].z, t[2].z, t[3].z, t[4].z));
+                    o.w = st_unsharp(iv[0].w, st_vblur1(t[0].w, t[1].w, t[2].w, t[3].w, t[4].w));
+                    if (x0 < W) stg_stream(reinterpret_cast<float4 *>(out + (long long)oy * W + x0), o);
+                }
+            }
+        }
+        // every lane is done reading slot d (its values fed the FMAs above)
+        __syncwarp();
+        if (lane == 0 && c + TS_D < nchunks) {
+            fence_proxy_async_smem();
+            issue(c + TS_D);
+        }
+    }
+    if (failed) {
+        if (lane == 0) atomicExch(status, kDeviceTimeout);
+        // let this warp's copies still in flight land before the CTA exits
+        const int last = min(nchunks, c + TS_D);
+        for (int k = c; k < last; ++k)
+            (void)mbar_wait_bounded(bar0 + 8 * (k % TS_D), (k / TS_D) & 1, timeout_ns);
+    }
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+cudaError_t launch_stencil_pipeline(const float *in, float *out, int H, int W, cudaStream_t st,
+                                    int drop_copy, unsigned long long timeout_ns)
+{
+    const bool aligned = ((reinterpret_cast<uintptr_t>(in) & 15) == 0) &&
+                         ((reinterpret_cast<uintptr_t>(out) & 15) == 0);
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    int *status = device_status_ptr();
+    if (aligned && (W % 4) == 0 && W >= TS_SW && H >= TS_RB && encode && status) {
+        CUtensorMap tm;
+        const cuuint64_t dims[2] = {(cuuint64_t)W, (cuuint64_t)H};
+        const cuuint64_t strides[1] = {(cuuint64_t)W * sizeof(float)};
+        const cuuint32_t box[2] = {TS_SW, TS_RB};
+        const cuuint32_t estr[2] = {1, 1};
+        CUresult r = encode(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(in), dims, strides, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r == CUDA_SUCCESS) {
+            const int nstrips = (W + ST_COLS_PER_WARP - 1) / ST_COLS_PER_WARP;
+            // about 16 warps per SM in one wave, bands of at least 16 rows
+            const long long want = 16LL * device_sm_count();
+            long long bands = (want + nstrips - 1) / nstrips;
+            const long long max_bands = (H + 15) / 16;
+            if (bands > max_bands) bands = max_bands;
+            if (bands < 1) bands = 1;
+            const int band = (int)((H + bands - 1) / bands);
+            const long long warps = (long long)nstrips * ((H + band - 1) / band);
+            const long long ctas = (warps + TS_WARPS - 1) / TS_WARPS;
+            if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+            stencil_tma_kernel<<<(unsigned)ctas, TS_WARPS * 32, 0, st>>>(tm, out, H, W, band, nstrips, status,
+                                                                         timeout_ns, drop_copy);
+            return cudaGetLastError();
+        }
+    }
+    if (drop_copy >= 0) return cudaErrorNotSupported;  // the test hook needs the TMA path
     const int col_tiles = (W + ST_COLS_PER_CTA - 1) / ST_COLS_PER_CTA;
     // Bands of rows: enough CTAs to keep every SM busy with several, but
     // tall enough that the 4 halo rows per band stay a small overhead.
@@ -163,9 +331,8 @@ cudaError_t launch_stencil_pipeline(const float *in, float *out, int H, int W, c
     const int rows = (int)((H + bands - 1) / bands);
     const long long nb = (long long)col_tiles * ((H + rows - 1) / rows);
     if (nb > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    const int vec = ((W & 3) == 0) && ((reinterpret_cast<uintptr_t>(in) & 15) == 0) &&
-                    ((reinterpret_cast<uintptr_t>(out) & 15) == 0);
-    stencil_pipeline_kernel<<<(unsigned)nb, ST_NWARPS * 32, 0, st>>>(in, out, H, W, rows, col_tiles, vec);
+    const int vec = ((W & 3) == 0) && aligned;
+    stencil_regs_kernel<<<(unsigned)nb, ST_NWARPS * 32, 0, st>>>(in, out, H, W, rows, col_tiles, vec);
     return cudaGetLastError();
 }
 

@@ -1,0 +1,29 @@
+"""Host-side pieces of bench.py (no GPU): argument parsing, the source files
+its profile-staleness hash reads, and the reference arm's oracle pass."""
+import os
+import sys
+
+import bench
+import synthetic as S
+
+
+def test_kernel_sources_exist():
+    for cid in (2, 3, 4):
+        for L in S.config(cid).layers:
+            for f in bench.kernel_sources(L):
+                assert os.path.exists(os.path.join(bench.ROOT, f)), f
+            assert len(bench.kernel_source_hash(bench.kernel_sources(L))) == 16
+
+
+def test_only_cases_cover_every_workload():
+    assert {c for c, _ in bench.ONLY_CASES.values()} == {1, 2, 3, 4, 5}
+
+
+def test_oracle_strip_pass_counts_pixels():
+    import oracle
+    wl = S.config(3, scale={"h": 16, "w": 24})
+    assert bench.oracle_net_pass(oracle, wl, 4) == 4 * 24
+
+
+def test_profiled_traffic_absent_or_stale_is_none():
+    assert bench.profiled_traffic("no-such-kernel", "0" * 16) is None

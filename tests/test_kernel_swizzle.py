@@ -64,53 +64,67 @@ def test_swz16_matches_the_page_formula(swz):
         assert swz.h_swz16(i, 3) == y * 8 + ((y ^ x) % 8)
 
 
-# (S, F_TB, W_T, TH, TW, C_SH): the tile table of dispatch_general<S>()
-GEN_TABLE = [(64, 8, 8, 32, 8), (32, 8, 8, 64, 8), (16, 4, 4, 64, 8), (8, 4, 4, 128, 8), (4, 8, 4, 256, 8)]
+# (F_TB, W_T, TH, TW): the tile table of dispatch_general<K>(); C_SH = 8 (4 for K = 7)
+GEN_TABLE = [(64, 8, 8, 32), (64, 7, 8, 28), (32, 8, 4, 64), (32, 7, 4, 56), (16, 4, 4, 64), (8, 4, 4, 128),
+             (4, 8, 4, 256)]
 
 
-def gen_cfg(S, F_TB, W_T, TH, TW, C_SH):
+def gen_cfg(K, F_TB, W_T, TH, TW):
     F_T = 8 if F_TB >= 8 else 4
     T_X = F_TB // F_T
     PXL = 32 // T_X
     WARP_COLS = PXL * W_T
+    C_SH = 4 if K >= 7 else 8
+    TWU = TW + K - 1
     return dict(F_T=F_T, T_X=T_X, PXL=PXL, WARP_COLS=WARP_COLS, WPR=TW // WARP_COLS,
-                NT=(TW // WARP_COLS) * TH * 32, TWP=TW + S - 1, CB=C_SH // 4)
+                NT=(TW // WARP_COLS) * TH * 32, TWU=TWU, TWP=(TWU + 7) // 8 * 8, CB=C_SH // 4,
+                THh=TH + K - 1)
 
 
-@pytest.mark.parametrize("S", [1, 3, 5, 7])
-@pytest.mark.parametrize("F_TB,W_T,TH,TW,C_SH", GEN_TABLE)
-def test_general_conv_pixel_reads_conflict_free(swz, S, F_TB, W_T, TH, TW, C_SH):
-    c = gen_cfg(S, F_TB, W_T, TH, TW, C_SH)
-    R = S
-    THh = TH + R - 1
+def col_map(swz, W_T, col):
+    """GenCfg::SWZ / phys_col<C>: XOR swizzle for even W_T, plain for odd."""
+    return swz.h_swz16(col, 3) if W_T % 2 == 0 else col
+
+
+@pytest.mark.parametrize("K", [1, 3, 5, 7])
+@pytest.mark.parametrize("F_TB,W_T,TH,TW", GEN_TABLE)
+def test_general_conv_pixel_reads_conflict_free(swz, K, F_TB, W_T, TH, TW):
+    c = gen_cfg(K, F_TB, W_T, TH, TW)
     for warp in range(c["NT"] // 32):
         ry = warp // c["WPR"]
         for cb in range(c["CB"]):
-            for r in range(R):
-                for j in range(W_T + S - 1):
+            for r in range(K):
+                for j in range(W_T + K - 1):
                     chunks = []
                     for lane in range(32):
                         pl = lane // c["T_X"]
                         cx0 = (warp % c["WPR"]) * c["WARP_COLS"] + pl * W_T
-                        base = (cb * THh + ry + r) * c["TWP"] + cx0
-                        chunks.append(swz.h_swz16(base + j, 3))
+                        row = cb * c["THh"] + ry + r
+                        chunks.append(row * c["TWP"] + col_map(swz, W_T, cx0 + j))
                     assert wavefronts_128bit(chunks) == min_wavefronts_128bit(chunks), \
                         (warp, cb, r, j)
 
 
-@pytest.mark.parametrize("S", [1, 3, 5, 7])
-@pytest.mark.parametrize("F_TB,W_T,TH,TW,C_SH", GEN_TABLE)
-def test_general_conv_tile_writes_conflict_free_and_bijective(swz, S, F_TB, W_T, TH, TW, C_SH):
-    c = gen_cfg(S, F_TB, W_T, TH, TW, C_SH)
-    nq = c["CB"] * (TH + S - 1) * c["TWP"]
-    allocated = (nq + 7) // 8 * 8          # GenCfg::in_chunks: padded to whole 8-chunk rows
-    phys = [swz.h_swz16(q, 3) for q in range(nq)]
-    assert len(set(phys)) == nq            # one-to-one
-    assert max(phys) < allocated           # never past the padded tile (the filter slice follows it)
-    for k in range(0, nq, c["NT"]):
-        for w0 in range(k, min(nq, k + c["NT"]), 32):
-            chunks = phys[w0:min(nq, w0 + 32)]
-            assert wavefronts_128bit(chunks) == min_wavefronts_128bit(chunks)
+@pytest.mark.parametrize("K", [1, 3, 5, 7])
+@pytest.mark.parametrize("F_TB,W_T,TH,TW", GEN_TABLE)
+def test_general_conv_tile_writes_stay_in_tile_and_are_one_to_one(swz, K, F_TB, W_T, TH, TW):
+    c = gen_cfg(K, F_TB, W_T, TH, TW)
+    # gen_issue_tile: warp copies whole tile rows, lane = column within the row
+    phys = []
+    for rowi in range(c["CB"] * c["THh"]):
+        for it in range(0, c["TWU"], 32):
+            chunks = [rowi * c["TWP"] + col_map(swz, W_T, xx) for xx in range(it, min(it + 32, c["TWU"]))]
+            assert wavefronts_128bit(chunks) == min_wavefronts_128bit(chunks)   # one warp instruction
+            phys += chunks
+    assert len(set(phys)) == len(phys) == c["CB"] * c["THh"] * c["TWU"]   # one-to-one
+    assert max(phys) < c["CB"] * c["THh"] * c["TWP"]                       # inside the stage's tile
+
+
+def test_odd_stride_needs_no_swizzle_and_xor_would_hurt(swz):
+    """W_T = 7: plain columns 7k are in 8 different bank groups; XORed ones are not."""
+    plain = [7 * k for k in range(8)]
+    assert wavefronts_128bit(plain) == 1
+    assert wavefronts_128bit([swz.h_swz16(cc, 3) for cc in plain]) > 1
 
 
 def test_general_conv_unswizzled_pixel_reads_would_conflict():

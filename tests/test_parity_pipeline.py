@@ -53,3 +53,25 @@ def test_constant_and_impulse(oracle_mod, cuda_dev, sc):
     img = np.zeros((50, 300), np.float32)
     img[20, 150] = 0.5
     assert np.abs(pipe_gpu(img, cuda_dev) - oracle_mod.stencil_pipeline(img)).max() <= PIPE_ATOL
+
+
+def test_bounded_wait_expiry_reports_status_and_context_survives(oracle_mod, cuda_dev, sc):
+    """Failure detection without a fault: one TMA copy is never issued, the
+    kernel's time-bounded wait for it expires (10 ms), it records
+    SC_ERR_DEVICE_TIMEOUT and returns; the next call works normally."""
+    img = S.uniform(51, 0, (64, 512), 0, 1)
+    ind = torch.from_numpy(img).to(cuda_dev)
+    outd = torch.empty_like(ind)
+    assert sc.sc_last_device_status() == sc.SC_OK
+    rc = sc.sc_test_stencil_wait_expiry(ind, outd, 64, 512, 1, 10000)
+    assert rc == sc.SC_OK, sc.sc_status_string(rc)
+    assert sc.sc_last_device_status() == sc.SC_ERR_DEVICE_TIMEOUT
+    assert sc.sc_last_device_status() == sc.SC_OK          # read clears it
+    out = pipe_gpu(img, cuda_dev)                            # context still usable
+    assert np.abs(out - oracle_mod.stencil_pipeline(img)).max() <= PIPE_ATOL
+
+
+def test_wait_expiry_hook_needs_the_tma_path(cuda_dev, sc):
+    ind = torch.zeros(8 * 100, device=cuda_dev)
+    outd = torch.empty_like(ind)
+    assert sc.sc_test_stencil_wait_expiry(ind, outd, 8, 100, 0, 1000) == sc.SC_ERR_UNSUPPORTED
