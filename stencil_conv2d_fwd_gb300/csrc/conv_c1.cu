@@ -13,6 +13,8 @@
 //    filter reads are broadcasts (Section 3.2.2 puts them in constant
 //    memory; here the CTA stages them once in shared memory, which gives
 //    the same broadcast without a per-call constant-bank upload).
+// The FMAs run as packed dual-FP32 FMAs (__ffma2_rn) on pairs of output
+// channels; each component rounds like fmaf.
 // Horizontal sharing between neighbouring threads goes through warp
 // shuffles instead of a shared-memory row: a lane's left and right halo
 // pixels are the edge values its neighbour lanes already hold in registers;
@@ -218,8 +220,20 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const float v = win[ky][j + kx];
+                    if constexpr (F_T % 2 == 0) {
+                        // packed FP32 FMA on pairs of output channels
+                        const float2 vv = make_float2(v, v);
 #pragma unroll
-                    for (int f = 0; f < F_T; ++f) acc[f][j] = fmaf(wv[f], v, acc[f][j]);
+                        for (int f = 0; f < F_T; f += 2) {
+                            float2 a2 = make_float2(acc[f][j], acc[f + 1][j]);
+                            a2 = __ffma2_rn(make_float2(wv[f], wv[f + 1]), vv, a2);
+                            acc[f][j] = a2.x;
+                            acc[f + 1][j] = a2.y;
+                        }
+                    } else {
+#pragma unroll
+                        for (int f = 0; f < F_T; ++f) acc[f][j] = fmaf(wv[f], v, acc[f][j]);
+                    }
                 }
             }
         }

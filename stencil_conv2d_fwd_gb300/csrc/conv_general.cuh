@@ -23,6 +23,11 @@
 // global->shared copy is one 16-byte cp.async with zero fill at the border.
 //
 // GB300 changes to the method:
+//  * The FMAs are issued as packed dual-FP32 FMAs (__ffma2_rn, sm_100 and
+//    later) on pairs of output channels: the two filter values come as one
+//    half of a 16-byte filter unit and the pixel value is used twice, so one
+//    instruction does two of the thread's FMAs.  Each component rounds like
+//    fmaf, so results equal the scalar-FMA kernel's.
 //  * Persistent CTAs: the grid is sized to the resident CTAs, and each CTA
 //    keeps its whole filter bank (all input channels, transposed to
 //    [ci][r][s][F_TB]) in shared memory for all the blocks it computes, when
@@ -257,8 +262,15 @@ __global__ void __launch_bounds__(C::NT, C::MINB)
                             for (int j = 0; j < C::W_T; ++j) {
                                 const float4 p = px[j + s];
                                 const float v = c == 0 ? p.x : (c == 1 ? p.y : (c == 2 ? p.z : p.w));
+                                const float2 vv = make_float2(v, v);
+                                // packed FP32 FMA on pairs of output channels
 #pragma unroll
-                                for (int f = 0; f < C::F_T; ++f) acc[f][j] = fmaf(wv[f], v, acc[f][j]);
+                                for (int f = 0; f < C::F_T; f += 2) {
+                                    float2 a2 = make_float2(acc[f][j], acc[f + 1][j]);
+                                    a2 = __ffma2_rn(make_float2(wv[f], wv[f + 1]), vv, a2);
+                                    acc[f][j] = a2.x;
+                                    acc[f + 1][j] = a2.y;
+                                }
                             }
                         }
                     }
