@@ -35,8 +35,8 @@
 //  * The kernel size is a template parameter K (square); an R x S filter
 //    with R, S <= K sits centred in the K x K taps with zeros around it.
 //
-// Shared-memory activation tile per stage: [C_SH/4][TH+K-1][TWP] chunks of
-// 16 bytes, TWP = TW + K - 1 rounded up to a multiple of 8.  The pixel lanes
+// Shared-memory activation tile per stage: C_SH/4 planes of [TH+K-1][TWP]
+// chunks of 16 bytes, TWP = TW + K - 1 rounded up to a multiple of 8.  The pixel lanes
 // of a warp read chunks W_T apart in one tile row.  For even W_T, chunk
 // `col` of a tile row is stored at column phys_col(col): inside each group of
 // 8 chunks (128 bytes) the chunk index is XORed with the group index, the
@@ -78,7 +78,10 @@ struct GenCfg {
     static constexpr int TWU = TW + K - 1;               // tile row width used
     static constexpr int TWP = (TWU + 7) & ~7;           // tile row pitch (chunks)
     static constexpr int WIN = W_T + K - 1;
-    static constexpr int IN_CHUNKS = CB * THh * TWP;     // multiple of 8
+    // Channel-block planes are THh * TWP + 2 chunks apart, so the planes of
+    // one pixel (copied by neighbouring lanes) start in different bank groups.
+    static constexpr int PLANE = THh * TWP + 2;
+    static constexpr int IN_CHUNKS = (CB * PLANE + 7) & ~7;
     static constexpr int STAGE_W = RESIDENT ? 0 : C_SH * KK * F_TB;
     static constexpr int STAGE_FLOATS = IN_CHUNKS * 4 + STAGE_W;
     static_assert(F_TB % F_T == 0 && 32 % T_X == 0, "bad channel split");
@@ -126,25 +129,25 @@ __device__ __forceinline__ void gen_issue_filters(float *ws, const float *__rest
 // Activation halo tile of output block (n, y0, x0), input channels
 // [c0, c0 + C_SH): one 16-byte cp.async per (channel block, row, column),
 // zero-filled outside the image and beyond Cin.  Each warp copies whole
-// tile rows, its lanes along the row, so the per-copy index arithmetic is a
-// few adds; 32 consecutive columns of a row never share a bank group.
+// tile rows; its lanes run over (column, channel block) with the channel
+// block fastest, so the 32 copies of one instruction read whole 32-byte
+// sectors of consecutive pixels (NHWC keeps a pixel's channels together)
+// and the per-copy index arithmetic stays a few adds.
 template <class C>
 __device__ __forceinline__ void gen_issue_tile(float4 *in_s, const float *__restrict__ x, int n, int y0,
                                                int x0, int c0, int H, int W, int Cin, int warp, int lane)
 {
-    for (int rowi = warp; rowi < C::CB * C::THh; rowi += C::NWARPS) {
-        const int cb = rowi / C::THh;
-        const int yy = rowi % C::THh;
+    for (int yy = warp; yy < C::THh; yy += C::NWARPS) {
         const int gy = y0 - C::K / 2 + yy;
-        const int ci = c0 + 4 * cb;
-        const bool row_ok = (gy >= 0) & (gy < H) & (ci < Cin);
-        const float *grow = x + ((((long long)n * H + (row_ok ? gy : 0)) * W) * Cin + (row_ok ? ci : 0));
-        float4 *srow = in_s + rowi * C::TWP;
-        for (int xx = lane; xx < C::TWU; xx += 32) {
+        const bool row_ok = (gy >= 0) & (gy < H);
+        const float *grow = x + ((((long long)n * H + (row_ok ? gy : 0)) * W) * Cin + c0);
+        for (int q = lane; q < C::TWU * C::CB; q += 32) {
+            const int cb = q % C::CB;
+            const int xx = q / C::CB;
             const int gx = x0 - C::K / 2 + xx;
-            const bool ok = row_ok & (gx >= 0) & (gx < W);
-            const float *src = ok ? grow + (long long)gx * Cin : x;
-            cp_async16(smem_u32(srow + phys_col<C>(xx)), src, ok ? 16 : 0);
+            const bool ok = row_ok & (gx >= 0) & (gx < W) & (c0 + 4 * cb < Cin);
+            const float *src = ok ? grow + (long long)gx * Cin + 4 * cb : x;
+            cp_async16(smem_u32(in_s + cb * C::PLANE + yy * C::TWP + phys_col<C>(xx)), src, ok ? 16 : 0);
         }
     }
 }
@@ -238,7 +241,7 @@ __global__ void __launch_bounds__(C::NT, C::MINB)
 #pragma unroll 1
                 for (int r = 0; r < C::K; ++r) {
                     // one input row: W_T + K - 1 pixels x 4 channels
-                    const float4 *row = in_s + (cb * C::THh + ry + r) * C::TWP;
+                    const float4 *row = in_s + cb * C::PLANE + (ry + r) * C::TWP;
                     float4 px[C::WIN];
 #pragma unroll
                     for (int j = 0; j < C::WIN; ++j) px[j] = row[pcol[j]];
@@ -363,26 +366,34 @@ cudaError_t launch_gen_auto(const ConvArgs &a, cudaStream_t st)
 // Columns computed beyond the image edge when rows are cut into tiles of tw.
 inline int tile_waste(int W, int tw) { return (W + tw - 1) / tw * tw - W; }
 
-// Tile table for kernel size K (measured on GB300 for 3x3 layers).  One CTA
-// per SM with 168 registers per thread beats two CTAs at 128: with fewer
-// registers the FFMA stream stalls more at dispatch.  The pixel run per
-// thread is 8 or 7, whichever wastes fewer columns at the image edge.
-template <int K>
-cudaError_t dispatch_general(const ConvArgs &a, cudaStream_t st)
+// Tiles for more than 16 output channels (measured on GB300, 3x3 layers).
+// One CTA per SM with ~160 registers per thread beats two CTAs at 128: with
+// fewer registers the FMA stream stalls more at dispatch.  The pixel run per
+// thread is 8 or 7, whichever wastes fewer columns at the image edge, and a
+// stage holds 16 input channels when Cin is a multiple of 16.
+template <int K, int CS>
+cudaError_t dispatch_wide(const ConvArgs &a, cudaStream_t st)
 {
-    // 7x7 filter slices staged per step need half the channels per stage
-    constexpr int CS = K >= 7 ? 4 : 8;
     if (a.Cout > 32) {
         if (tile_waste(a.W, 28) < tile_waste(a.W, 32)) return launch_gen_auto<K, 64, 7, 8, 28, CS, 1>(a, st);
         return launch_gen_auto<K, 64, 8, 8, 32, CS, 1>(a, st);
     }
-    if (a.Cout > 16) {
-        if (tile_waste(a.W, 56) < tile_waste(a.W, 64)) return launch_gen_auto<K, 32, 7, 4, 56, CS, 1>(a, st);
-        return launch_gen_auto<K, 32, 8, 4, 64, CS, 1>(a, st);
-    }
+    if (tile_waste(a.W, 56) < tile_waste(a.W, 64)) return launch_gen_auto<K, 32, 7, 8, 56, CS, 1>(a, st);
+    return launch_gen_auto<K, 32, 8, 8, 64, CS, 1>(a, st);
+}
+
+// Tiles for 16 or fewer output channels.
+template <int K, int CS>
+cudaError_t dispatch_narrow(const ConvArgs &a, cudaStream_t st)
+{
     if (a.Cout > 8) return launch_gen_auto<K, 16, 4, 4, 64, CS, 2>(a, st);
     if (a.Cout > 4) return launch_gen_auto<K, 8, 4, 4, 128, CS, 2>(a, st);
-    return launch_gen_auto<K, 4, 8, 4, 256, CS, 2>(a, st);
+    return launch_gen_auto<K, 4, 4, 4, 128, CS, 2>(a, st);
 }
+
+// Channels per stage: 16 when Cin is a multiple of 16 (3x3 only), else 8;
+// 7x7 filter slices staged per step need 4.
+template <int K>
+constexpr int stage_channels_small() { return K >= 7 ? 4 : 8; }
 
 }  // namespace sc

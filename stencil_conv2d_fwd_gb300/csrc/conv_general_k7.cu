@@ -3,5 +3,9 @@
 #include "conv_general.cuh"
 
 namespace sc {
-cudaError_t launch_conv_general_k7(const ConvArgs &a, cudaStream_t st) { return dispatch_general<7>(a, st); }
+cudaError_t launch_conv_general_k7(const ConvArgs &a, cudaStream_t st)
+{
+    constexpr int CS = stage_channels_small<7>();
+    return a.Cout > 16 ? dispatch_wide<7, CS>(a, st) : dispatch_narrow<7, CS>(a, st);
+}
 }  // namespace sc
