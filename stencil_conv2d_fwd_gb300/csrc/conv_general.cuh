@@ -36,14 +36,14 @@
 //    with R, S <= K sits centred in the K x K taps with zeros around it.
 //
 // Shared-memory activation tile per stage: C_SH/4 planes of [TH+K-1][TWP]
-// chunks of 16 bytes, TWP = TW + K - 1 rounded up to a multiple of 8.  The pixel lanes
-// of a warp read chunks W_T apart in one tile row.  For even W_T, chunk
-// `col` of a tile row is stored at column phys_col(col): inside each group of
-// 8 chunks (128 bytes) the chunk index is XORed with the group index, the
-// swizzle of "CUDA共有メモリのスウィズリング" with 128-byte swizzle rows, which
-// puts those lanes in different bank groups with a constant key per lane.
-// For odd W_T the plain layout is already conflict-free (and the XOR would
-// not be).
+// chunks of 16 bytes, TWP = TW + K - 1 rounded up to a multiple of 8.  The
+// pixel lanes of a warp read chunks W_T apart in one tile row.  Chunk `col`
+// of a tile row is stored at column phys_col(col): inside each group of 8
+// chunks (128 bytes) the chunk index is XORed with the group index, the
+// swizzle of "CUDA共有メモリのスウィズリング" with 128-byte swizzle rows, keeping
+// as many low bits of the group index as the lane stride needs (none for odd
+// W_T, whose plain layout is already conflict-free).  Each lane's key is a
+// constant over the run.
 #pragma once
 
 #include "common.cuh"
@@ -61,9 +61,12 @@ struct GenCfg {
     static constexpr int C_SH = C_SH_;
     static constexpr bool RESIDENT = RESIDENT_;
     static constexpr int MINB = MINB_;                   // CTAs per SM the registers must allow
-    // Pixel lanes read chunks W_T apart.  An odd stride already spreads 8
-    // lanes over 8 bank groups; an even one needs the XOR swizzle.
-    static constexpr bool SWZ = (W_T % 2) == 0;
+    // Pixel lanes read chunks W_T apart, and a 16-byte shared load is served
+    // 8 lanes at a time.  An odd stride already puts 8 lanes in 8 bank groups;
+    // a stride of 2, 4 or 8 needs the chunk index XORed with the low 1, 2 or
+    // 3 bits of its 8-chunk group index (SWZ_MASK), which makes any 8
+    // consecutive lanes conflict-free for every kernel size.
+    static constexpr int SWZ_MASK = (W_T % 8 == 0) ? 7 : (W_T % 4 == 0) ? 3 : (W_T % 2 == 0) ? 1 : 0;
     static constexpr int F_T = F_TB >= 8 ? 8 : 4;       // output channels per thread
     static constexpr int NG = F_T / 4;                   // float4 groups per thread
     static constexpr int T_X = F_TB / F_T;               // lanes along output channels
@@ -78,9 +81,10 @@ struct GenCfg {
     static constexpr int TWU = TW + K - 1;               // tile row width used
     static constexpr int TWP = (TWU + 7) & ~7;           // tile row pitch (chunks)
     static constexpr int WIN = W_T + K - 1;
-    // Channel-block planes are THh * TWP + 2 chunks apart, so the planes of
-    // one pixel (copied by neighbouring lanes) start in different bank groups.
-    static constexpr int PLANE = THh * TWP + 2;
+    // Channel-block planes are THh * TWP + 8 / CB chunks apart: the 8 lanes
+    // of one copy phase hold 8 / CB consecutive pixels x CB blocks, and the
+    // stagger puts each block's pixels in their own bank groups.
+    static constexpr int PLANE = THh * TWP + (CB >= 8 ? 1 : 8 / CB);
     static constexpr int IN_CHUNKS = (CB * PLANE + 7) & ~7;
     static constexpr int STAGE_W = RESIDENT ? 0 : C_SH * KK * F_TB;
     static constexpr int STAGE_FLOATS = IN_CHUNKS * 4 + STAGE_W;
@@ -97,9 +101,14 @@ struct GenCfg {
     static size_t smem_bytes(int cin_pad) { return (w_res_floats(cin_pad) + 2 * (size_t)STAGE_FLOATS) * 4; }
 };
 
-// Physical chunk column of logical chunk column `col` in a tile row.
+// Physical chunk column of logical chunk column `col` in a tile row: inside
+// each group of 8 chunks (128 bytes), the chunk index XOR the low bits of
+// the group index.
 template <class C>
-__host__ __device__ __forceinline__ int phys_col(int col) { return C::SWZ ? swz16(col, 3) : col; }
+__host__ __device__ __forceinline__ int phys_col(int col)
+{
+    return (col & ~7) | ((col ^ ((col >> 3) & C::SWZ_MASK)) & 7);
+}
 
 // Copy filters for input channels [c0, c0 + nci) into ws[(ci-c0)*KK + r*K + s][F_TB]
 // (transposed, output channels contiguous), zero where the R x S filter has

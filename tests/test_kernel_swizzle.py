@@ -48,6 +48,16 @@ def min_wavefronts_128bit(chunks):
     return -(-len(set(chunks)) // 8)
 
 
+def phases_conflict_free(chunks_by_lane):
+    """A 16-byte shared access is served 8 lanes at a time: in each group of 8
+    consecutive lanes, distinct chunks must sit in distinct bank groups."""
+    for q in range(0, len(chunks_by_lane), 8):
+        ph = set(chunks_by_lane[q:q + 8])
+        if len({c % 8 for c in ph}) != len(ph):
+            return False
+    return True
+
+
 @pytest.mark.parametrize("L", [1, 2, 3, 4, 5])
 def test_swz16_is_a_bijection_per_row(swz, L):
     n = 1 << L
@@ -81,12 +91,15 @@ def gen_cfg(K, F_TB, W_T, TH, TW, C_SH):
     TWU = TW + K - 1
     return dict(F_T=F_T, T_X=T_X, PXL=PXL, WARP_COLS=WARP_COLS, WPR=TW // WARP_COLS,
                 NT=(TW // WARP_COLS) * TH * 32, TWU=TWU, TWP=(TWU + 7) // 8 * 8, CB=C_SH // 4,
-                THh=TH + K - 1, PLANE=(TH + K - 1) * ((TWU + 7) // 8 * 8) + 2)
+                THh=TH + K - 1,
+                PLANE=(TH + K - 1) * ((TWU + 7) // 8 * 8) + (1 if C_SH >= 32 else 8 // (C_SH // 4)))
 
 
 def col_map(swz, W_T, col):
-    """GenCfg::SWZ / phys_col<C>: XOR swizzle for even W_T, plain for odd."""
-    return swz.h_swz16(col, 3) if W_T % 2 == 0 else col
+    """phys_col<C>: XOR with the low bits of the 8-chunk group index, as many
+    bits as the lane stride W_T needs (GenCfg::SWZ_MASK)."""
+    m = 7 if W_T % 8 == 0 else 3 if W_T % 4 == 0 else 1 if W_T % 2 == 0 else 0
+    return (col & ~7) | ((col ^ ((col >> 3) & m)) & 7)
 
 
 @pytest.mark.parametrize("K", [1, 3, 5, 7])
@@ -105,6 +118,7 @@ def test_general_conv_pixel_reads_conflict_free(swz, K, F_TB, W_T, TH, TW, C_SH)
                         chunks.append(cb * c["PLANE"] + (ry + r) * c["TWP"] + col_map(swz, W_T, cx0 + j))
                     assert wavefronts_128bit(chunks) == min_wavefronts_128bit(chunks), \
                         (warp, cb, r, j)
+                    assert phases_conflict_free(chunks), (warp, cb, r, j)
 
 
 @pytest.mark.parametrize("K", [1, 3, 5, 7])
@@ -120,10 +134,13 @@ def test_general_conv_tile_writes_stay_in_tile_and_are_one_to_one(swz, K, F_TB, 
             for q in qs[it:it + 32]:
                 cb, xx = q % c["CB"], q // c["CB"]
                 chunks.append(cb * c["PLANE"] + yy * c["TWP"] + col_map(swz, W_T, xx))
-            # one warp instruction: conflict-free when all 32 lanes copy; the
-            # partial last instruction of a row takes at most one extra wavefront
+            # one warp instruction: conflict-free when all 32 lanes copy, and in
+            # every 8-lane phase; the partial last instruction of a row may take
+            # one extra wavefront
             slack = 0 if len(chunks) == 32 else 1
             assert wavefronts_128bit(chunks) <= min_wavefronts_128bit(chunks) + slack
+            if len(chunks) == 32:
+                assert phases_conflict_free(chunks)
             phys += chunks
     assert len(set(phys)) == len(phys) == c["CB"] * c["THh"] * c["TWU"]   # one-to-one
     assert max(phys) < (c["CB"] * c["PLANE"] + 7) // 8 * 8                 # inside the stage's tile
