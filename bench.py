@@ -42,6 +42,7 @@ FP32_LANES_PER_SM = 128          # FP32 FMA lanes per Blackwell SM (4 schedulers
 # --only cases: (workload id, layer index; None = the stencil pipeline)
 ONLY_CASES = {
     "1": (1, 0), "2": (2, 0), "3-L1": (3, 0), "3-L2": (3, 1), "3-L3": (3, 2), "4": (4, 0), "5": (5, None),
+    "4-tc": (4, 0), "3-L2-tc": (3, 1),
 }
 
 
@@ -429,6 +430,36 @@ def per_config(sc, S, dev, stream, flush, fp32_tflops, hbm_gbs, hbm_src):
     c4 = S.config(4)
     conv_entry("4: N=32 56x56 64->64 3x3", 32, 56, 56, c4.layers[0], c4.x.transpose(0, 2, 3, 1))
 
+    # tensor-core (tcgen05, TF32) variant, reported separately: its own
+    # tolerance (5e-3 * sum|x*w|) and its own roofline (TF32 tensor peak)
+    peaks = measured_peaks() or {}
+    tf32_tflops = float(peaks.get("bf16_tflops", 1900.0)) * 1.1 / 2.25
+    for name, cid, li in (("4 (tcgen05 TF32)", 4, 0), ("3-L2 (tcgen05 TF32)", 3, 1), ("3-L3 (tcgen05 TF32)", 3, 2)):
+        wl = S.config(cid)
+        L = wl.layers[li]
+        xin = wl.x if li == 0 else np.maximum(S.uniform(77, 0, (wl.n, L.cin, wl.h, wl.w), -1, 1), 0)
+        xd = torch.from_numpy(np.ascontiguousarray(xin.transpose(0, 2, 3, 1)).astype(np.float32)).to(dev)
+        wd, bd = torch.from_numpy(L.w).to(dev), torch.from_numpy(L.b).to(dev)
+        yd = torch.empty(wl.n * wl.h * wl.w * L.cout, device=dev)
+
+        def call_tc(s=None):
+            rc = sc.conv2d_fwd_tc(xd, wd, bd, yd, wl.n, wl.h, wl.w, L.cin, L.cout, L.r, L.s, L.act,
+                                  s if s is not None else stream)
+            if rc != 0:
+                raise RuntimeError(sc.sc_status_string(rc))
+        med, mn = time_events(call_tc, stream, flush, reps=20)
+        flops = conv_flops(wl.n, wl.h, wl.w, L)
+        byts = 4 * (wl.n * wl.h * wl.w * (L.cin + L.cout) + L.w.size + L.b.size)
+        t_c, t_m = flops / (tf32_tflops * 1e12), byts / (hbm_gbs * 1e9)
+        out[name] = {"ms_median": round(med, 5), "ms_min": round(mn, 5),
+                     "gflops": round(flops / (med * 1e-3) / 1e9, 2),
+                     "mpixel_per_s": round(wl.n * wl.h * wl.w / (med * 1e-3) / 1e6, 2),
+                     "roofline_bound": "tensor" if t_c >= t_m else "hbm",
+                     "roofline_us": round(max(t_c, t_m) * 1e6, 3),
+                     "roofline_frac": round(max(t_c, t_m) / (med * 1e-3), 4),
+                     "tolerance": "5e-3 * sum|x*w| (TF32 operands)",
+                     "tf32_peak_tflops": round(tf32_tflops, 1)}
+
     c5 = S.config(5)
     ind = torch.from_numpy(c5.img).to(dev)
     outd = torch.empty_like(ind)
@@ -563,7 +594,10 @@ def run_only(args, local):
             if k < li:
                 sc.check(sc.conv2d_fwd(x, wd, bd, y, N, H, W, L.cin, L.cout, L.r, L.s, sc.SC_NHWC, L.act))
                 x = y
-        launch = lambda: sc.conv2d_fwd(x, wd, bd, y, N, H, W, L.cin, L.cout, L.r, L.s, sc.SC_NHWC, L.act)
+        if args.only.endswith("-tc"):   # the tensor-core (TF32) variant
+            launch = lambda: sc.conv2d_fwd_tc(x, wd, bd, y, N, H, W, L.cin, L.cout, L.r, L.s, L.act)
+        else:
+            launch = lambda: sc.conv2d_fwd(x, wd, bd, y, N, H, W, L.cin, L.cout, L.r, L.s, sc.SC_NHWC, L.act)
     for _ in range(args.warmup + args.steps):
         sc.check(launch())
     torch.cuda.synchronize()

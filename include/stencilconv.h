@@ -69,6 +69,23 @@ int conv2d_fwd(const float *x, const float *w, const float *b, float *y,
                int layout, int act, sc_stream_t stream);
 
 /*
+ * conv2d_fwd_tc: the same operation as conv2d_fwd on the tensor cores
+ * (tcgen05 MMA, accumulators in tensor memory) as an implicit GEMM
+ * (pixels x output channels x (taps, input channels); "Optimizing Memory
+ * Efficiency for Convolution Kernels on Kepler GPUs", Section 3.3, sets
+ * this GEMM formulation against direct convolution).  x and w enter the
+ * MMA as TF32 (10 explicit mantissa bits), products accumulate in fp32, so
+ * results differ from conv2d_fwd by up to about 5e-3 * sum|x * w| per
+ * element: a separate variant with its own tolerance, not a replacement.
+ * x, y : NHWC, 16-byte aligned.  w : OIHW.  b : Cout floats or NULL.
+ * Supported: Cin % 4 == 0, Cout % 4 == 0, Cout <= 128, R and S odd and <= 3.
+ * Returns SC_OK or a negative sc_status (SC_ERR_UNSUPPORTED outside that).
+ */
+int conv2d_fwd_tc(const float *x, const float *w, const float *b, float *y,
+                  int N, int H, int W, int Cin, int Cout, int R, int S,
+                  int act, sc_stream_t stream);
+
+/*
  * stencil_pipeline_fwd: three stencil stages fused in one pass over a
  * single-channel image ("Model-Based Warp Overlapped Tiling for Image
  * Processing Programs on GPUs", Abstract: stages fused into overlapped

@@ -36,6 +36,7 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int
 SIGNATURES = {
     "conv2d_fwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
+    "conv2d_fwd_tc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "stencil_pipeline_fwd": (_I, [_P, _P, _I, _I, _P]),
     "sc_repack": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "sc_last_device_status": (_I, [_P]),
@@ -100,6 +101,12 @@ def _stream(s) -> Optional[int]:
 def conv2d_fwd(x, w, b, y, N, H, W, Cin, Cout, R, S, layout=SC_NHWC, act=SC_ACT_NONE, stream=None) -> int:
     return load().conv2d_fwd(_ptr(x), _ptr(w), _ptr(b), _ptr(y), N, H, W, Cin, Cout, R, S,
                              layout, act, _stream(stream))
+
+
+def conv2d_fwd_tc(x, w, b, y, N, H, W, Cin, Cout, R, S, act=SC_ACT_NONE, stream=None) -> int:
+    """Tensor-core (TF32) variant of conv2d_fwd, NHWC only (see the header)."""
+    return load().conv2d_fwd_tc(_ptr(x), _ptr(w), _ptr(b), _ptr(y), N, H, W, Cin, Cout, R, S, act,
+                                _stream(stream))
 
 
 def stencil_pipeline_fwd(inp, out, H, W, stream=None) -> int:

@@ -156,6 +156,30 @@ int conv2d_fwd(const float *x, const float *w, const float *b, float *y, int N, 
     return rc;
 }
 
+int conv2d_fwd_tc(const float *x, const float *w, const float *b, float *y, int N, int H, int W, int Cin,
+                  int Cout, int R, int S, int act, sc_stream_t stream)
+{
+    if (!x || !w || !y) return SC_ERR_NULL;
+    const long long nx = checked_count({N, H, W, Cin});
+    const long long ny = checked_count({N, H, W, Cout});
+    const long long nw = checked_count({Cout, Cin, R, S});
+    if (nx < 0 || ny < 0 || nw < 0) return SC_ERR_SHAPE;
+    if (H > (1 << 30) || W > (1 << 30)) return SC_ERR_SHAPE;
+    if ((R & 1) == 0 || (S & 1) == 0 || R > 3 || S > 3) return SC_ERR_UNSUPPORTED;
+    if (act != SC_ACT_NONE && act != SC_ACT_RELU) return SC_ERR_UNSUPPORTED;
+    if ((Cin % 4) != 0 || (Cout % 4) != 0 || Cout > 128) return SC_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(y)) return SC_ERR_ALIGN;
+    const size_t ybytes = (size_t)ny * sizeof(float);
+    if (overlaps(y, ybytes, x, (size_t)nx * sizeof(float)) ||
+        overlaps(y, ybytes, w, (size_t)nw * sizeof(float)) ||
+        overlaps(y, ybytes, b, b ? (size_t)Cout * sizeof(float) : 0))
+        return SC_ERR_ALIAS;
+    sc::ConvArgs a{x, w, b, y, N, H, W, Cin, Cout, R, S, act};
+    const cudaError_t e = sc::launch_conv_tc(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return SC_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? SC_OK : cuda_fail(e);
+}
+
 int stencil_pipeline_fwd(const float *in, float *out, int H, int W, sc_stream_t stream)
 {
     if (!in || !out) return SC_ERR_NULL;

@@ -25,6 +25,10 @@ cudaError_t launch_conv_general_k7(const ConvArgs &a, cudaStream_t st);
 // kernel for K = max(R, S) (api.cu).
 cudaError_t launch_conv_nhwc(const ConvArgs &a, cudaStream_t st);
 
+// Tensor-core (tcgen05, TF32) implicit-GEMM convolution, NHWC, Cin % 4 == 0,
+// Cout <= 128, R, S <= 3 (conv_tc.cu).  cudaErrorNotSupported otherwise.
+cudaError_t launch_conv_tc(const ConvArgs &a, cudaStream_t st);
+
 // Single-input-channel convolution, Cout == 1 or Cout % 4 == 0 (conv_c1.cu).
 cudaError_t launch_conv_c1(const ConvArgs &a, cudaStream_t st);
 
