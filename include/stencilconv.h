@@ -60,8 +60,9 @@ typedef enum { SC_ACT_NONE = 0, SC_ACT_RELU = 1 } sc_act;
  *   Cout % 4 == 0.  x and y 16-byte aligned for Cin > 1 (NHWC vectors of 4
  *   channels).  Anything else returns SC_ERR_UNSUPPORTED / SC_ERR_ALIGN.
  * SC_NCHW with more than one channel on either side goes through the
- *   repack kernels and a stream-ordered temporary buffer (cudaMallocAsync on
- *   `stream`, freed on `stream` after use).
+ *   repack kernels and a stream-ordered temporary buffer (allocated on
+ *   `stream` from the library's memory pool, freed on `stream` after use;
+ *   see sc_release_workspace).
  * Returns SC_OK or a negative sc_status.
  */
 int conv2d_fwd(const float *x, const float *w, const float *b, float *y,
@@ -77,9 +78,15 @@ int conv2d_fwd(const float *x, const float *w, const float *b, float *y,
  * MMA as TF32 (10 explicit mantissa bits), products accumulate in fp32, so
  * results differ from conv2d_fwd by up to about 5e-3 * sum|x * w| per
  * element: a separate variant with its own tolerance, not a replacement.
- * x, y : NHWC, 16-byte aligned.  w : OIHW.  b : Cout floats or NULL.
- * Supported: Cin % 4 == 0, Cout % 4 == 0, Cout <= 128, R and S odd and <= 3.
- * Returns SC_OK or a negative sc_status (SC_ERR_UNSUPPORTED outside that).
+ * x, y : NHWC, 16-byte aligned.  w : OIHW, 16-byte aligned.  b : Cout
+ *   floats or NULL.
+ * Supported: Cin % 4 == 0, Cout % 4 == 0, Cout <= 128, R and S odd and <= 3,
+ *   and filters small enough to stay resident in shared memory: each CTA
+ *   holds the filters of a group of up to 32 output channels (and, while it
+ *   starts, a second copy in OIHW order), so the group shrinks to 16, 8 or
+ *   4 channels as Cin grows; beyond Cin of about 500, SC_ERR_UNSUPPORTED.
+ * Returns SC_OK or a negative sc_status (SC_ERR_UNSUPPORTED outside that,
+ *   SC_ERR_ALIGN for unaligned pointers).
  */
 int conv2d_fwd_tc(const float *x, const float *w, const float *b, float *y,
                   int N, int H, int W, int Cin, int Cout, int R, int S,
@@ -138,6 +145,16 @@ int sc_measure_ffma_peak(float *sink, int blocks, int iters, sc_stream_t stream)
 
 /* sc_version: library version as 10000*major + 100*minor + patch. */
 int sc_version(void);
+
+/*
+ * sc_release_workspace: hand the memory of the library's temporary buffers
+ * back to the driver.  Those buffers (the NCHW repack of conv2d_fwd) come
+ * from a library-private
+ * stream-ordered memory pool per device that otherwise keeps freed memory
+ * for the next call.  Memory still in use by queued work is not affected.
+ * Returns SC_OK.
+ */
+int sc_release_workspace(void);
 
 /*
  * sc_test_stencil_wait_expiry: test hook for the device-status path, not

@@ -44,6 +44,7 @@ SIGNATURES = {
     "sc_last_cuda_error": (_I, []),
     "sc_measure_ffma_peak": (_I, [_P, _I, _I, _P]),
     "sc_version": (_I, []),
+    "sc_release_workspace": (_I, []),
     "conv2d_fwd_nchw_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "sc_test_stencil_wait_expiry": (_I, [_P, _P, _I, _I, _I, _I, _P]),
 }
@@ -138,6 +139,11 @@ def sc_measure_ffma_peak(sink, blocks, iters, stream=None) -> int:
 
 def sc_version() -> int:
     return load().sc_version()
+
+
+def sc_release_workspace() -> int:
+    """Trim the library's pool of temporary device buffers (see the header)."""
+    return load().sc_release_workspace()
 
 
 def conv2d_fwd_nchw_noalloc(x, w, b, y, N, H, W, Cin, Cout, R, S, act=SC_ACT_NONE, stream=None) -> int:

@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <cstring>
 #include <initializer_list>
+#include <mutex>
 
 #include "../../include/stencilconv.h"
 #include "launch.h"
@@ -80,6 +81,58 @@ int *device_status_ptr()
     return addr[dev];
 }
 
+// Temporary buffers come from one library-private memory pool per device
+// whose release threshold is unlimited: memory freed on a stream stays in
+// the pool for the next call, where the default pool would hand it back to
+// the driver at the next synchronisation and map it again on the next
+// allocation.  sc_release_workspace() trims the pools.
+static std::mutex g_pool_mu;
+static cudaMemPool_t g_pool[64] = {};
+
+static cudaError_t workspace_pool(cudaMemPool_t *out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_pool_mu);
+    if (!g_pool[dev]) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        e = cudaMemPoolCreate(&pool, &props);
+        if (e != cudaSuccess) return e;
+        uint64_t keep = ~0ull;
+        e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        if (e != cudaSuccess) {
+            cudaMemPoolDestroy(pool);
+            return e;
+        }
+        g_pool[dev] = pool;
+    }
+    *out = g_pool[dev];
+    return cudaSuccess;
+}
+
+cudaError_t workspace_alloc(void **p, size_t bytes, cudaStream_t st)
+{
+    cudaMemPool_t pool = nullptr;
+    const cudaError_t e = workspace_pool(&pool);
+    if (e != cudaSuccess) return e;
+    return cudaMallocFromPoolAsync(p, bytes, pool, st);
+}
+
+cudaError_t workspace_free(void *p, cudaStream_t st) { return cudaFreeAsync(p, st); }
+
+void workspace_trim()
+{
+    std::lock_guard<std::mutex> lock(g_pool_mu);
+    for (cudaMemPool_t pool : g_pool)
+        if (pool) cudaMemPoolTrimTo(pool, 0);
+}
+
 int device_sm_count()
 {
     static int cached[64] = {0};
@@ -133,7 +186,7 @@ int conv2d_fwd(const float *x, const float *w, const float *b, float *y, int N, 
     const size_t out_bytes = need_out ? (size_t)ny * sizeof(float) : 0;
     const size_t off = (in_bytes + 255) & ~(size_t)255;
     void *ws = nullptr;
-    cudaError_t e = cudaMallocAsync(&ws, off + out_bytes, st);
+    cudaError_t e = sc::workspace_alloc(&ws, off + out_bytes, st);
     if (e != cudaSuccess) return cuda_fail(e);
     float *x_nhwc = need_in ? static_cast<float *>(ws) : nullptr;
     float *y_nhwc = need_out ? reinterpret_cast<float *>(static_cast<char *>(ws) + off) : y;
@@ -151,7 +204,7 @@ int conv2d_fwd(const float *x, const float *w, const float *b, float *y, int N, 
         e = sc::launch_transpose_batched(y_nhwc, y, N, (long long)H * W, Cout, st);
         if (e != cudaSuccess) rc = cuda_fail(e);
     }
-    cudaError_t ef = cudaFreeAsync(ws, st);
+    cudaError_t ef = sc::workspace_free(ws, st);
     if (rc == SC_OK && ef != cudaSuccess) rc = cuda_fail(ef);
     return rc;
 }
@@ -168,7 +221,7 @@ int conv2d_fwd_tc(const float *x, const float *w, const float *b, float *y, int 
     if ((R & 1) == 0 || (S & 1) == 0 || R > 3 || S > 3) return SC_ERR_UNSUPPORTED;
     if (act != SC_ACT_NONE && act != SC_ACT_RELU) return SC_ERR_UNSUPPORTED;
     if ((Cin % 4) != 0 || (Cout % 4) != 0 || Cout > 128) return SC_ERR_UNSUPPORTED;
-    if (!aligned16(x) || !aligned16(y)) return SC_ERR_ALIGN;
+    if (!aligned16(x) || !aligned16(y) || !aligned16(w)) return SC_ERR_ALIGN;
     const size_t ybytes = (size_t)ny * sizeof(float);
     if (overlaps(y, ybytes, x, (size_t)nx * sizeof(float)) ||
         overlaps(y, ybytes, w, (size_t)nw * sizeof(float)) ||
@@ -252,6 +305,12 @@ int sc_measure_ffma_peak(float *sink, int blocks, int iters, sc_stream_t stream)
 }
 
 int sc_version(void) { return 100; }
+
+int sc_release_workspace(void)
+{
+    sc::workspace_trim();
+    return SC_OK;
+}
 
 int sc_test_stencil_wait_expiry(const float *in, float *out, int H, int W, int drop_copy, int timeout_us,
                                 sc_stream_t stream)

@@ -1,56 +1,73 @@
 // Tensor-core variant of the direct convolution: implicit GEMM on the 5th
 // generation tensor cores (tcgen05, accumulators in tensor memory), TF32
 // operands, fp32 accumulation.  It computes the same operation as
-// conv2d_fwd (stride 1, zero "same" padding, bias, ReLU) with TF32 rounding
-// of x and w, so it is checked with its own tolerance (5e-3 * sum|x*w|).
+// conv2d_fwd (stride 1, zero "same" padding, bias, ReLU; R, S in {1, 3}) with
+// TF32 rounding of x and w, so it is checked with its own tolerance
+// (5e-3 * sum|x*w|).
 //
-// GEMM view: D[pixel][co] = sum_{r,s,ci} A[pixel][(r,s,ci)] * B[co][(r,s,ci)],
-// A[p][(r,s,ci)] = x at pixel p shifted by (r - R/2, s - S/2), channel ci.
-// ("Optimizing Memory Efficiency for Convolution Kernels on Kepler GPUs",
-// Section 3.3, compares direct convolution with this GEMM formulation; the
-// reuse argument of Section 3.3.2 is kept: each input pixel is staged once
-// per tile, and every tap reads it again from shared memory.)
+// GEMM view ("Optimizing Memory Efficiency for Convolution Kernels on Kepler
+// GPUs", Section 3.3, compares direct convolution with the GEMM
+// formulation; the reuse argument of Section 3.3.2 is kept: each input pixel
+// is staged once per tile and every tap reads it again from shared memory).
+// With 3 x 3 taps (r, s) and a group of Cg output channels per CTA:
 //
-// Tile: TR x TC output pixels x N output channels (N = Cout rounded up to
-// 16, at most 64; larger Cout runs as channel groups on blockIdx.y).  Shared memory holds the tile's halo as "padded pixels" with row pitch
-// WP = TC + K - 1: padded pixel q = ty * WP + tx is image pixel
-// (y0 + ty - K/2, x0 + tx - K/2), zero outside the image.  Output pixel
-// (ty, tx) of the tile is GEMM row m = ty * WP + tx, and its tap (r, s) reads
-// padded pixel m + r * WP + s: the A operand of tap (r, s) is the same
-// staged data starting r * WP + s pixels later, so a tap is only a different
-// start address in the MMA's shared-memory descriptor.  Rows m with
-// tx >= TC are computed and discarded (K - 1 of every WP).
+//   D_mt[m][(s, co)] = sum_r sum_ci A[mt*128 + r*WP + m][ci] * w[co][ci][r][s]
+//   y[pixel m of M-tile mt][co] = sum_s D_mt[m + s][(s, co)]
 //
-// Operand layouts (K-major, no swizzle): the canonical core matrix is 8 rows
-// x 16 bytes.  A: a plane of padded pixels per 4-channel block, 16 bytes per
-// pixel, so 8 consecutive pixels form a core matrix (SBO = 128 bytes) and the
-// next 4 channels are the next plane (LBO = plane stride).  B (filters): per
-// tap and 4-channel block, the Cout rows of 16 bytes (SBO 128, LBO N * 16).
-// One MMA is M = 128 rows x N x K = 8 (two 4-channel blocks).
+// A holds the tile's padded pixels (row pitch WP = 32: padded pixel
+// q = py * 32 + px is image pixel (y0 - 1 + py, x0 - 1 + px), zero outside
+// the image), so the vertical tap r is an A start address r * WP rows
+// further, while the three horizontal taps s sit side by side in the MMA's N
+// dimension (N = 3 * Cg rounded up to 16).  Stacking the taps in N instead of
+// issuing one MMA per tap matters because an M = 128 MMA costs about
+// (A bytes + B bytes) / 128 B per clock of shared-memory reads, at least
+// ~44 clocks, whatever N: with N = Cg <= 64 the tensor core would stay below
+// two thirds of its rate.  The sum over s is a shift by s GEMM rows, i.e. by
+// s TMEM lanes: the epilogue adds the columns of lane l + s with a warp
+// shuffle.  Output column tx of a tile is lane tx of a warp; with WP = 32
+// each warp's 32 lanes are one padded image row and lanes 30 and 31 (which
+// would need the next warp's lanes) are exactly the two padding columns, so
+// a tile is TC = 30 output columns wide and 4 image rows per M-tile.
 //
-// Pipeline: persistent CTAs (one per SM), each with its whole filter bank
-// resident in shared memory, and warp-specialised roles linked by
+// Operand layouts (K-major): A is staged 32 channels at a time by one 4-D TMA
+// box per stage with 128-byte swizzling: one 128-byte row per padded pixel,
+// 8-row atoms (SBO = 1024 bytes); a K step of 8 channels is +32 bytes of the
+// start address, a vertical tap +4 KB, an M-tile +16 KB, so every start
+// address keeps the swizzle phase of its 1024-byte-aligned stage buffer.  B
+// (filters, no swizzle): per (8-channel step, r), two 4-channel blocks of N
+// rows x 16 bytes (core matrices of 8 rows, SBO 128 bytes, LBO N * 16 bytes);
+// row n = s * Cg + co.  One MMA is M = 128 x N x K = 8.
+//
+// Pipeline: persistent CTAs (one per SM and channel group), the group's
+// filter bank resident in shared memory, warp-specialised roles linked by
 // mbarriers:
-//  * producer (warp 4, one lane): per stage, two 4-D TMA copies
-//    (cp.async.bulk.tensor) of the tile's padded activations, one box of
-//    (4 channels, WP pixels, TR+K-1 rows) per channel-block plane; the TMA
-//    zero fill outside the image is the convolution's zero padding.  A stage
-//    buffer is refilled once the MMAs that read it have completed (`empty`).
+//  * all warps first stage the group's filters (bulk copy of the OIHW rows,
+//    then a transpose in shared memory into the B layout).
+//  * producer (warp 4, one lane): per stage one TMA box of (32 channels, 32 pixels, TR + 2 rows) of the
+//    tile's padded activations; the TMA zero fill outside the image (and
+//    past Cin) is the convolution's zero padding.  A stage buffer is
+//    refilled once the MMAs that read it have completed (`empty`).
 //  * MMA issuer (warp 5, one lane): waits for a stage (`full`), issues its
-//    K*K*MT MMAs, commits them to the stage's `empty` barrier, and after a
-//    tile's last stage commits to the tile's accumulator barrier.
+//    (K steps) x 3 x MT MMAs, commits them to the stage's `empty` barrier,
+//    and after a tile's last stage commits to the tile's accumulator
+//    barrier.  Each barrier wait leaves the tensor core idle for ~100-200
+//    clocks, so stages are large (32 channels).
 //  * epilogue (warps 0-3, one TMEM lane quadrant each): waits for a tile's
-//    accumulators, reads them with tcgen05.ld, adds bias, applies ReLU,
-//    writes NHWC, and frees the accumulator buffer.  Accumulators are
-//    double-buffered in tensor memory, so a tile's epilogue overlaps the
-//    next tile's MMAs.
+//    accumulators, reads the three s-blocks with tcgen05.ld, sums them with
+//    lane shifts, transposes through a swizzled per-warp shared-memory
+//    buffer so that each store instruction writes whole pixel records, adds
+//    bias, applies ReLU, writes NHWC, and frees the accumulator buffer.
+//    Accumulators are double-buffered in tensor memory, so a tile's epilogue
+//    overlaps the next tile's MMAs.
 // Every wait is bounded in time; on expiry the CTA records
 // SC_ERR_DEVICE_TIMEOUT, lets its own copies and MMAs land, frees tensor
 // memory and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
@@ -60,16 +77,14 @@ namespace sc {
 namespace tc {
 
 constexpr int NTHREADS = 192;   // warps 0-3 epilogue (TMEM lane quadrants), 4 producer, 5 MMA
-constexpr int NSTAGE = 3;       // activation stages in flight
+constexpr int WP = 32;          // padded row pitch (pixels) = lanes of a warp
+constexpr int TC = 30;          // output columns per tile
+constexpr int CH = 32;          // channels per stage (one 128-byte swizzled row per pixel)
+constexpr int MIN_STAGE = 2;
+constexpr int MAX_STAGE = 6;
 constexpr int TMEM_BUF = 256;   // tensor-memory columns per accumulator buffer (two buffers)
-
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo)
-{
-    // start address, LBO, SBO in 16-byte units; version 1 (bits 46-47);
-    // base offset 0; layout type 0 = no swizzle (bits 61-63)
-    return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46);
-}
+constexpr int OUT_BUF = 4096;                // one epilogue output buffer: 30 pixel rows of up to 128 bytes
+constexpr int STG_BYTES = 4 * 2 * OUT_BUF;   // two per epilogue warp
 
 // Instruction descriptor, kind::tf32: D = F32, A = B = TF32, both K-major,
 // dense, M = 128.
@@ -78,15 +93,28 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int n)
     return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n >> 3) << 17) | ((128u >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
+// Shared-memory matrix descriptors as two 32-bit words: low = start address
+// (16-byte units, bits 0-13) | LBO (16-byte units) << 16; high = SBO
+// (16-byte units) | version 1 << 14 | layout type << 29 (bits 61-63 of the
+// descriptor; 0 = no swizzle, 2 = 128-byte swizzle); base offset 0.  Shared
+// addresses stay below 2^18, so stepping a start address is one 32-bit add
+// that cannot carry into the LBO field.
+constexpr uint32_t A_HI = (1024u >> 4) | (1u << 14) | (2u << 29);
+constexpr uint32_t B_HI = (128u >> 4) | (1u << 14);
+
+__device__ __forceinline__ void mma_tf32_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo, uint32_t b_hi,
+                                           uint32_t idesc, uint32_t acc)
 {
     asm volatile(
         "{\n"
         ".reg .pred p;\n"
-        "setp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n"
+        ".reg .b64 da, db;\n"
+        "setp.ne.b32 p, %6, 0;\n"
+        "mov.b64 da, {%1, %2};\n"
+        "mov.b64 db, {%3, %4};\n"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], da, db, %5, p;\n"
         "}\n" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc)
         : "memory");
 }
 
@@ -111,51 +139,117 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
 __device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
 __device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
 
-// 16 consecutive fp32 TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+// CW consecutive fp32 TMEM columns (4, 8, 16 or 32) of this thread's lane;
+// the caller waits with tmem_wait_ld before using them.
+template <int CW>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[CW])
 {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+    if constexpr (CW == 4) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];\n"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                     : "r"(taddr));
+    } else if constexpr (CW == 8) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                     : "r"(taddr));
+    } else if constexpr (CW == 16) {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+            : "r"(taddr));
+    } else {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+            "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+              "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+              "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+              "=r"(r[30]), "=r"(r[31])
+            : "r"(taddr));
+    }
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d)
+{
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
+// Swizzle key of pixel row p of an epilogue output buffer (rows of CW
+// floats, 1024-byte aligned): 16-byte chunk q of row p is stored at chunk
+// q ^ key(p).  This is the TMA's own 128-byte (CW = 32) or 64-byte (CW = 16)
+// swizzle pattern, so the buffer is a valid source for a swizzled TMA store,
+// and the row-wise writes (one row per lane) of every 8-lane phase touch 8
+// distinct 16-byte bank groups.
+template <int CW>
+__device__ __forceinline__ int stg_key(int p)
+{
+    return CW == 32 ? (p & 7) : ((p >> 1) & 3);
 }
 
 struct TcGeom {
-    int TC, TR, WP, THh, MT, P;  // tile cols/rows, padded pitch, padded rows, M-tiles, pixels per plane
-    int tiles_x, tiles_y, ntiles, nk;
-    uint32_t a_plane_bytes, a_bytes, box_bytes, w_bytes, smem_bytes, tmem_cols;
+    int MT, TR, THh;                // M-tiles per tile, tile rows (4 * MT), staged rows (TR + 2)
+    int tiles_x, tiles_y, ntiles;   // tiles of TC x TR output pixels, per image and in all
+    int nk, nstg, nstage;           // 8-channel K steps, 32-channel stages per tile, stage buffers
+    int raw_pitch;                  // 16-byte units per output channel of the staged OIHW filters
+    uint32_t stage_bytes, w_bytes, smem_bytes, tmem_cols;
 };
 
 }  // namespace tc
 
-// N: output channels per CTA (multiple of 16, <= 64), K: kernel size.
-template <int K, int N>
+__device__ __forceinline__ void give_up_flag(int &flag) { atomicExch(&flag, 1); }
+
+// CG: output channels per CTA (4, 8, 16 or 32); NB = MMA N = 3 * CG rounded
+// up to 16.
+template <int CG>
 __global__ void __launch_bounds__(tc::NTHREADS, 1)
-    conv_tc_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restrict__ w,
-                   const float *__restrict__ bias, float *__restrict__ y, int Nimg, int H, int W, int Cin, int Cout,
-                   int R, int S, int act, tc::TcGeom g, int *status, unsigned long long timeout_ns)
+    conv_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmy,
+                   const float *__restrict__ w, const float *__restrict__ bias, float *__restrict__ y, int H, int W,
+                   int Cin, int Cout, int R, int S, int act, tc::TcGeom g, int *status, unsigned long long timeout_ns)
 {
-    extern __shared__ __align__(1024) unsigned char smem_raw[];
-    __shared__ __align__(8) unsigned long long full_bar[tc::NSTAGE], empty_bar[tc::NSTAGE];
-    __shared__ __align__(8) unsigned long long acc_full[2], acc_empty[2];
+    constexpr int NB = (3 * CG + 15) / 16 * 16;
+    constexpr int CW = CG;                         // epilogue column chunk = the group
+    constexpr bool TMA_OUT = CW >= 16;             // store through a shared-memory buffer and TMA
+    constexpr int CPR = CW / 4;                    // 16-byte chunks per pixel
+    extern __shared__ __align__(1024) unsigned char smem_dyn[];
+    __shared__ __align__(8) unsigned long long full_bar[tc::MAX_STAGE], empty_bar[tc::MAX_STAGE];
+    __shared__ __align__(8) unsigned long long acc_full[2], acc_empty[2], w_bar, wt_bar;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int dr = (K - R) / 2, ds = (K - S) / 2;
-    const int co0 = blockIdx.y * N;                      // this CTA's output channels co0 .. co0+N-1
-    unsigned char *wsm = smem_raw;                       // resident filters
-    unsigned char *abuf = smem_raw + g.w_bytes;          // NSTAGE activation stages
+    const int co0 = blockIdx.y * CG;                     // this CTA's output channels co0 .. co0+CG-1
+    const int ns = g.nstage;
+    // stage buffers need 1024-byte alignment (the 128-byte swizzle pattern)
+    unsigned char *smem_raw = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
+    unsigned char *abuf = smem_raw;                      // ns activation stages
+    unsigned char *wsm = abuf + (size_t)ns * g.stage_bytes;   // resident filters
+    unsigned char *stg = wsm + g.w_bytes;                // epilogue transpose buffers
 
+    // Filters, once per CTA.  The producer warp bulk-copies the group's OIHW
+    // weights (one contiguous run of Cin * R * S floats per output channel)
+    // into the top of the stage buffers, rows g.raw_pitch 16-byte units apart
+    // (an odd number, so that the 16-byte reads below are free of bank
+    // conflicts); warps 0-3 and 5 then rearrange them into the MMA's B
+    // layout: the [k][r][cb][n][4] bank whose element (k, r, cb, n, j) with
+    // n = s * CG + co is w[co0 + co][8k + 4cb + j][r - (3 - R) / 2][s - (3 - S) / 2],
+    // zero for n >= 3 * CG, taps the R x S filter lacks, channels beyond Cin
+    // and co beyond Cout.  One unit is one output channel and one block of 4
+    // input channels; neighbouring lanes take neighbouring output channels,
+    // whose B rows are neighbours.  Meanwhile the producer already fills the
+    // stage buffers below the staged weights; `wt_bar` (one arrive per
+    // rearranging warp) releases the rest, and the bank, to the MMA warp.
+    const int RS = R * S;
+    const int co_n = Cout - co0 < CG ? Cout - co0 : CG;   // output channels this CTA copies
+    const uint32_t raw_bytes = (uint32_t)(CG * g.raw_pitch * 16);
+    unsigned char *raw_sm = abuf + (size_t)ns * g.stage_bytes - raw_bytes;
     if (warp == 0) tc::tmem_alloc(smem_u32(&tmem_base_sh), g.tmem_cols);
     if (tid == 0) {
-        for (int j = 0; j < tc::NSTAGE; ++j) {
+        for (int j = 0; j < ns; ++j) {
             mbar_init(smem_u32(&full_bar[j]), 1);
             mbar_init(smem_u32(&empty_bar[j]), 1);
         }
@@ -163,89 +257,146 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
             mbar_init(smem_u32(&acc_full[j]), 1);
             mbar_init(smem_u32(&acc_empty[j]), 4);   // one arrive per epilogue warp
         }
+        mbar_init(smem_u32(&w_bar), 1);
+        mbar_init(smem_u32(&wt_bar), 5);
         abort_sh = 0;
         fence_mbar_init();
     }
-    // Filters, once per CTA, as asynchronous 4-byte copies: element
-    // (k, tap, cb, co, j) of the [stage][tap][cb][co][4] bank is input
-    // channel 8k + 4cb + j; taps the R x S filter lacks, channels beyond Cin
-    // and co beyond Cout read zero.  The overhang of every activation plane
-    // (pixels past the TMA box, read only by discarded GEMM rows) is zeroed.
-    {
-        float *wf = reinterpret_cast<float *>(wsm);
-        const int n_e = (int)(g.w_bytes / 4);
-        const int RS = R * S;
-        for (int e = tid; e < n_e; e += tc::NTHREADS) {
-            const int j = e & 3;
-            int t2 = e >> 2;
-            const int co = t2 % N;
-            t2 /= N;
-            const int cb = t2 & 1;
-            t2 >>= 1;
-            const int tap = t2 % (K * K);
-            const int k = t2 / (K * K);
-            const int ci = 8 * k + 4 * cb + j;
-            const int r = tap / K - dr, s = tap % K - ds;
-            const bool ok = (k < g.nk) & (ci < Cin) & (co0 + co < Cout) & (r >= 0) & (r < R) & (s >= 0) & (s < S);
-            const float *src = ok ? w + ((size_t)(co0 + co) * Cin + ci) * RS + r * S + s : w;
-            cp_async4(smem_u32(wf + e), src, ok ? 4 : 0);
-        }
-        cp_async_commit();
-        float4 *af = reinterpret_cast<float4 *>(abuf);
-        const int used = g.THh * g.WP;
-        for (int e = tid; e < tc::NSTAGE * 2 * g.P; e += tc::NTHREADS) {
-            if (e % g.P >= used) af[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        cp_async_wait<0>();
-    }
-    fence_proxy_async_smem();   // generic-proxy writes above -> visible to the tensor core
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = tmem_base_sh;
+    if (warp == 4) {
+        const uint32_t row = (uint32_t)(Cin * RS * 4);
+        if (lane == 0) mbar_arrive_expect_tx(smem_u32(&w_bar), row * (uint32_t)co_n);
+        __syncwarp();
+        for (int co = lane; co < co_n; co += 32)
+            bulk_load(smem_u32(raw_sm) + (uint32_t)(co * g.raw_pitch * 16), w + (size_t)(co0 + co) * Cin * RS, row,
+                      smem_u32(&w_bar));
+    } else {
+        const bool landed = mbar_wait_bounded(smem_u32(&w_bar), 0, timeout_ns);
+        if (!landed) give_up_flag(abort_sh);
+        const float *raw = reinterpret_cast<const float *>(raw_sm);
+        float4 *bank = reinterpret_cast<float4 *>(wsm);
+        constexpr int LT = tc::NTHREADS - 32;   // threads of warps 0-3 and 5
+        const int lt = warp < 4 ? tid : tid - 32;
+        const int units = CG * 2 * g.nk;
+        for (int u = lt; landed && u < units; u += LT) {
+            const int co = u % CG, cib = u / CG;
+            const int k = cib >> 1, cb = cib & 1;
+            const bool ok = co < co_n && 4 * cib < Cin;
+            const float *src = raw + (size_t)co * g.raw_pitch * 4 + (size_t)4 * cib * RS;   // [j][rr][ss]
+            float f[36];   // [j][r][s] of the 3 x 3 taps
+            if (R == 3 && S == 3) {
+#pragma unroll
+                for (int q = 0; q < 9; ++q) {
+                    const float4 v = ok ? *reinterpret_cast<const float4 *>(src + 4 * q) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    f[4 * q] = v.x;
+                    f[4 * q + 1] = v.y;
+                    f[4 * q + 2] = v.z;
+                    f[4 * q + 3] = v.w;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int t = 0; t < 9; ++t) {
+                        const int rr = t / 3 - (3 - R) / 2, ss = t % 3 - (3 - S) / 2;
+                        f[j * 9 + t] = (ok && rr >= 0 && rr < R && ss >= 0 && ss < S) ? src[j * RS + rr * S + ss] : 0.f;
+                    }
+            }
+#pragma unroll
+            for (int t = 0; t < 9; ++t) {
+                const int r = t / 3, s = t % 3;
+                bank[((k * 3 + r) * 2 + cb) * NB + s * CG + co] = make_float4(f[t], f[9 + t], f[18 + t], f[27 + t]);
+            }
+        }
+        // B rows n >= 3 * CG (N rounded up to a multiple of 16) are zero
+        constexpr int PADN = NB - 3 * CG;
+        if constexpr (PADN > 0) {
+            for (int e = lt; e < g.nk * 3 * 2 * PADN; e += LT)
+                bank[(e / PADN) * NB + 3 * CG + e % PADN] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        // the staged weights' buffers go to the TMA (async proxy) next, the
+        // bank to the tensor core
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&wt_bar));
+    }
 
     const int my_tiles = (g.ntiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
-    const int total = my_tiles * g.nk;
+    const int total = my_tiles * g.nstg;
     auto tile_origin = [&](int u, int &n, int &y0, int &x0) {
         int t = (int)blockIdx.x + u * (int)gridDim.x;
-        x0 = (t % g.tiles_x) * g.TC;
+        x0 = (t % g.tiles_x) * tc::TC;
         t /= g.tiles_x;
         y0 = (t % g.tiles_y) * g.TR;
         n = t / g.tiles_y;
     };
     auto aborted = [&]() { return *reinterpret_cast<volatile int *>(&abort_sh) != 0; };
-    auto give_up = [&]() { atomicExch(&abort_sh, 1); };
+    auto give_up = [&]() { give_up_flag(abort_sh); };
 
     if (warp == 4) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            int issued = 0;
+            int issued = 0, s = 0, c = 0, u = 0;
+            uint32_t ph = 0;
+            int n, y0, x0;
+            tile_origin(0, n, y0, x0);
+            const int first_raw = (int)((ns * g.stage_bytes - raw_bytes) / g.stage_bytes);   // lowest buffer under the staged weights
             for (int j = 0; j < total && !aborted(); ++j) {
-                const int s = j % tc::NSTAGE;
-                if (j >= tc::NSTAGE &&
-                    !mbar_wait_bounded(smem_u32(&empty_bar[s]), ((j / tc::NSTAGE) - 1) & 1, timeout_ns)) {
+                if (j >= ns && !mbar_wait_bounded(smem_u32(&empty_bar[s]), ph ^ 1u, timeout_ns)) {
                     give_up();
                     break;
                 }
-                int n, y0, x0;
-                tile_origin(j / g.nk, n, y0, x0);
-                const int c = 8 * (j % g.nk);
-                unsigned char *st = abuf + s * g.a_bytes;
-                mbar_arrive_expect_tx(smem_u32(&full_bar[s]), 2 * g.box_bytes);
-                tma_load_4d(smem_u32(st), &tmx, c, x0 - K / 2, y0 - K / 2, n, smem_u32(&full_bar[s]));
-                tma_load_4d(smem_u32(st + g.a_plane_bytes), &tmx, c + 4, x0 - K / 2, y0 - K / 2, n,
+                if (j == first_raw && !mbar_wait_bounded(smem_u32(&wt_bar), 0, timeout_ns)) {
+                    give_up();
+                    break;
+                }
+                mbar_arrive_expect_tx(smem_u32(&full_bar[s]), g.stage_bytes);
+                tma_load_4d(smem_u32(abuf + (size_t)s * g.stage_bytes), &tmx, tc::CH * c, x0 - 1, y0 - 1, n,
                             smem_u32(&full_bar[s]));
                 issued = j + 1;
+                if (++s == ns) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+                if (++c == g.nstg) {
+                    c = 0;
+                    if (++u < my_tiles) tile_origin(u, n, y0, x0);
+                }
             }
             // every copy this lane issued has landed before the CTA may exit
-            for (int j = (issued > tc::NSTAGE ? issued - tc::NSTAGE : 0); j < issued; ++j)
-                (void)mbar_wait_bounded(smem_u32(&full_bar[j % tc::NSTAGE]), (j / tc::NSTAGE) & 1, timeout_ns);
+            for (int j = (issued > ns ? issued - ns : 0); j < issued; ++j)
+                (void)mbar_wait_bounded(smem_u32(&full_bar[j % ns]), (j / ns) & 1, timeout_ns);
         }
     } else if (warp == 5) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = tc::idesc_tf32(N);
-            int j = 0, committed = -1;
+            constexpr uint32_t idesc = tc::idesc_tf32(NB);
+            const uint32_t a_base = smem_u32(abuf) >> 4, w_base = smem_u32(wsm) >> 4;
+            const uint32_t a_lbo = 1u << 16, b_lbo = (uint32_t)NB << 16;
+            // G M-tiles at a time, M-tiles innermost: consecutive MMAs go to
+            // different accumulators (back-to-back MMAs into one accumulator
+            // issue more slowly).  A: +2 units (32 B) per K step, +256 units
+            // (4 KB) per vertical tap, +1024 units (16 KB) per M-tile.  B:
+            // 2 * NB units per (K step, tap).
+            auto issue = [&](auto gsz, uint32_t d0, uint32_t a0, uint32_t b0, int nks, uint32_t acc0) {
+                constexpr int G = decltype(gsz)::value;
+#pragma unroll 1
+                for (int kk = 0; kk < nks; ++kk) {
+#pragma unroll
+                    for (int r = 0; r < 3; ++r)
+#pragma unroll
+                        for (int gi = 0; gi < G; ++gi)
+                            tc::mma_tf32_w(d0 + (uint32_t)(gi * NB), a0 + (uint32_t)(kk * 2 + r * 256 + gi * 1024),
+                                           tc::A_HI, b0 + (uint32_t)((kk * 3 + r) * 2 * NB), tc::B_HI, idesc,
+                                           (kk > 0 || r > 0) ? 1u : acc0);
+                }
+            };
+            int s = 0, j = 0, committed = -1;
+            uint32_t ph = 0;
+            if (!mbar_wait_bounded(smem_u32(&wt_bar), 0, timeout_ns)) give_up();   // the bank is complete
             for (int u = 0; u < my_tiles && !aborted(); ++u) {
                 const int b = u & 1;
                 if (u >= 2 && !mbar_wait_bounded(smem_u32(&acc_empty[b]), ((u >> 1) - 1) & 1, timeout_ns)) {
@@ -255,29 +406,34 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
                 tc::fence_after_sync();
                 const uint32_t dbase = tmem + (uint32_t)(b * tc::TMEM_BUF);
                 bool ok = true;
-                for (int k = 0; k < g.nk; ++k, ++j) {
-                    const int s = j % tc::NSTAGE;
-                    if (!mbar_wait_bounded(smem_u32(&full_bar[s]), (j / tc::NSTAGE) & 1, timeout_ns)) {
+                for (int c = 0; c < g.nstg; ++c, ++j) {
+                    if (!mbar_wait_bounded(smem_u32(&full_bar[s]), ph, timeout_ns)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after_sync();
-                    // descriptors advance by adding 16-byte units to the start-address field
-                    const uint64_t a_desc0 = tc::smem_desc(smem_u32(abuf + s * g.a_bytes), g.a_plane_bytes, 128);
-                    const uint64_t b_desc0 =
-                        tc::smem_desc(smem_u32(wsm + (size_t)k * K * K * 2 * N * 16), N * 16, 128);
-#pragma unroll
-                    for (int tap = 0; tap < K * K; ++tap) {
-                        const int r = tap / K, sx = tap % K;
-                        const uint64_t bd = b_desc0 + (uint64_t)(tap * 2 * N);
-                        const uint64_t ad_tap = a_desc0 + (uint64_t)(r * g.WP + sx);
-#pragma unroll 1
-                        for (int mt = 0; mt < g.MT; ++mt)
-                            tc::mma_tf32(dbase + (uint32_t)(mt * N), ad_tap + (uint64_t)(mt * 128), bd, idesc,
-                                         (k > 0 || tap > 0) ? 1u : 0u);
+                    const uint32_t a_lo = (a_base + (uint32_t)s * (g.stage_bytes >> 4)) | a_lbo;
+                    const uint32_t b_lo = (w_base + (uint32_t)(c * 4 * 3 * 2 * NB)) | b_lbo;
+                    const int nks = g.nk - 4 * c < 4 ? g.nk - 4 * c : 4;
+                    const uint32_t acc0 = c > 0 ? 1u : 0u;
+                    int mt = 0;
+                    if (g.MT == 1) {
+                        issue(std::integral_constant<int, 1>{}, dbase, a_lo, b_lo, nks, acc0);
+                        mt = 1;
+                    } else if (g.MT & 1) {
+                        issue(std::integral_constant<int, 3>{}, dbase, a_lo, b_lo, nks, acc0);
+                        mt = 3;
                     }
+#pragma unroll 1
+                    for (; mt < g.MT; mt += 2)
+                        issue(std::integral_constant<int, 2>{}, dbase + (uint32_t)(mt * NB), a_lo + (uint32_t)(mt * 1024),
+                              b_lo, nks, acc0);
                     tc::mma_commit(smem_u32(&empty_bar[s]));
                     committed = j;
+                    if (++s == ns) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
                 if (!ok) {
                     give_up();
@@ -287,13 +443,28 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
             }
             // MMAs still executing must finish before tensor memory is freed
             if (committed >= 0)
-                (void)mbar_wait_bounded(smem_u32(&empty_bar[committed % tc::NSTAGE]),
-                                        (committed / tc::NSTAGE) & 1, timeout_ns);
+                (void)mbar_wait_bounded(smem_u32(&empty_bar[committed % ns]), (committed / ns) & 1, timeout_ns);
         }
     } else if (warp < 4) {
         // ------------------------------------------------------------ epilogue
+        // Lane l of warp w holds GEMM row m = mt * 128 + 32 w + l, i.e. padded
+        // column l of tile row 4 mt + w; its output column l (l < 30) is the
+        // sum over s of the s-block of lane l + s.  With TMA_OUT each lane
+        // writes its pixel (bias and ReLU applied) into the warp's output
+        // buffer and lane 0 stores the row with one TMA copy (image edges and
+        // channels past Cout are clipped by the TMA); the warp's two buffers
+        // alternate, lane 0 waiting for the store that last read one before
+        // it is refilled.  Otherwise (CW of 4 or 8 channels, 16 or 32 bytes
+        // per pixel) each lane stores its pixel directly: neighbouring lanes
+        // write neighbouring pixels.
+        float bias_r[CW];
+#pragma unroll
+        for (int i = 0; i < CW; ++i) bias_r[i] = (bias && co0 + i < Cout) ? __ldg(bias + co0 + i) : 0.f;
+        const uint32_t wst = smem_u32(stg + warp * 2 * tc::OUT_BUF);
+        int nstore = 0;
         for (int u = 0; u < my_tiles; ++u) {
             const int b = u & 1;
+            if (aborted()) break;
             const bool got = mbar_wait_bounded(smem_u32(&acc_full[b]), (u >> 1) & 1, timeout_ns);
             if (__any_sync(0xffffffffu, !got) || aborted()) {
                 if (lane == 0) give_up();
@@ -304,107 +475,122 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
             tile_origin(u, n, y0, x0);
             const uint32_t tbuf = tmem + (uint32_t)(b * tc::TMEM_BUF) + ((uint32_t)(warp * 32) << 16);
             for (int mt = 0; mt < g.MT; ++mt) {
-                const int m = mt * 128 + warp * 32 + lane;
-                const int ty = m / g.WP, tx = m % g.WP;
-                const int oy = y0 + ty, ox = x0 + tx;
-                const bool valid = (ty < g.TR) & (tx < g.TC) & (oy < H) & (ox < W);
-                float *yp = y + ((((long long)n * H + (valid ? oy : 0)) * W + (valid ? ox : 0)) * Cout + co0);
-#pragma unroll 1
-                for (int c0 = 0; c0 < N; c0 += 16) {
-                    float v[16];
-                    tc::tmem_ld16(tbuf + (uint32_t)(mt * N + c0), v);
-                    if (valid) {
+                uint32_t r0[CW], r1[CW], r2[CW];
+                tc::tmem_ld<CW>(tbuf + (uint32_t)(mt * NB), r0);
+                tc::tmem_ld<CW>(tbuf + (uint32_t)(mt * NB + CG), r1);
+                tc::tmem_ld<CW>(tbuf + (uint32_t)(mt * NB + 2 * CG), r2);
+                tc::tmem_wait_ld();
+                if (mt == g.MT - 1) {
+                    // every column of this buffer is in registers: release it
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&acc_empty[b]));
+                }
+                float v[CW];
 #pragma unroll
-                        for (int q = 0; q < 16; q += 4) {
-                            const int co = c0 + q;             // within the group
-                            if (co0 + co < Cout) {
-                                const float *bq = bias ? bias + co0 + co : nullptr;
-                                float4 o;
-                                o.x = relu_if(v[q + 0] + (bq ? __ldg(bq + 0) : 0.f), act);
-                                o.y = relu_if(v[q + 1] + (bq ? __ldg(bq + 1) : 0.f), act);
-                                o.z = relu_if(v[q + 2] + (bq ? __ldg(bq + 2) : 0.f), act);
-                                o.w = relu_if(v[q + 3] + (bq ? __ldg(bq + 3) : 0.f), act);
-                                *reinterpret_cast<float4 *>(yp + co) = o;
-                            }
-                        }
+                for (int i = 0; i < CW; ++i)
+                    v[i] = relu_if(__uint_as_float(r0[i]) + __shfl_down_sync(0xffffffffu, __uint_as_float(r1[i]), 1) +
+                                       __shfl_down_sync(0xffffffffu, __uint_as_float(r2[i]), 2) + bias_r[i],
+                                   act);
+                const int oy = y0 + mt * 4 + warp;
+                if (oy >= H) continue;   // the same for the whole warp
+                if constexpr (TMA_OUT) {
+                    const uint32_t ob = wst + (uint32_t)((nstore & 1) * tc::OUT_BUF);
+                    if (lane == 0) bulk_wait_read<1>();   // the store that last read this buffer is done
+                    __syncwarp();
+                    if (lane < tc::TC) {
+#pragma unroll
+                        for (int q = 0; q < CPR; ++q)
+                            tc::st_shared_v4(ob + lane * (CW * 4) + ((q ^ tc::stg_key<CW>(lane)) << 4), v[4 * q],
+                                             v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    }
+                    fence_proxy_async_smem();   // these writes -> visible to the TMA
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_4d(&tmy, ob, co0, x0, oy, n);
+                        bulk_commit();
+                    }
+                    ++nstore;
+                } else {
+                    const int ox = x0 + lane;
+                    if (lane < tc::TC && ox < W) {
+                        float *yp = y + (((long long)n * H + oy) * W + ox) * Cout + co0;
+#pragma unroll
+                        for (int q = 0; q < CPR; ++q)
+                            if (co0 + 4 * q < Cout)
+                                *reinterpret_cast<float4 *>(yp + 4 * q) =
+                                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                     }
                 }
             }
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&acc_empty[b]));
         }
+        if (TMA_OUT && lane == 0) bulk_wait_all();   // every store has written global memory
     }
 
     tc::fence_before_sync();
     __syncthreads();
+    if (tid == 0) (void)mbar_wait_bounded(smem_u32(&w_bar), 0, timeout_ns);   // the weight copies have landed
     if (aborted() && tid == 0 && status) atomicExch(status, kDeviceTimeout);
     if (warp == 0) tc::tmem_dealloc(tmem, g.tmem_cols);
 }
 
-// Padded pixels per channel-block plane: every pixel the MMAs read (the
-// last GEMM row plus the largest tap offset), rounded to a multiple of 8 so
-// each plane starts 128-byte aligned (a TMA destination).
-static int tc_plane_pixels(int MT, int K, int WP)
-{
-    const int need = MT * 128 + (K - 1) * WP + (K - 1);
-    return (need + 7) / 8 * 8;
-}
+// Largest dynamic shared memory a CTA may use (227 KB less a margin for the
+// static barriers), of which 1 KB may go to aligning the stage buffers.
+constexpr size_t kTcSmemCap = 227 * 1024 - 1024;
 
-// Tile geometry: pitch WP = TC + K - 1; M-tiles of 128 GEMM rows; TR rows
-// so that MT * N fits the 512 tensor-memory columns and the resident filters
-// plus two activation stages fit in shared memory.
-static bool tc_geometry(int K, int N, int groups, int Cin, int H, int W, int Nimg, tc::TcGeom &g)
+// Tile geometry for output-channel groups of Cg (MMA N = NB): M-tiles of 4
+// image rows x 32 padded columns; MT M-tiles per tile so that MT * NB fits one
+// accumulator buffer and at least MIN_STAGE stage buffers of (4 MT + 2) rows
+// fit in shared memory beside the filters and the epilogue buffers; among
+// those, the MT that wastes least work on halo rows, partial tiles and an
+// unevenly filled persistent grid.  Leftover shared memory goes to further
+// stage buffers (up to MAX_STAGE).
+static bool tc_geometry(int Cg, int NB, int groups, int Cin, int RS, int H, int W, int Nimg, tc::TcGeom &g)
 {
     const int nk = (Cin + 7) / 8;
-    const size_t w_bytes = (size_t)nk * K * K * 2 * N * 16;
-    if (w_bytes > 160 * 1024) return false;
-    int best_tc = -1, best_tr = 0;
+    const size_t w_bytes = ((size_t)nk * 3 * 2 * NB * 16 + 1023) & ~(size_t)1023;
+    const size_t fixed = w_bytes + tc::STG_BYTES + 1024;   // + alignment slack
+    if (fixed >= kTcSmemCap) return false;
+    const int sms = device_sm_count() / groups > 0 ? device_sm_count() / groups : 1;   // CTAs per channel group
+    const int tiles_x = (W + tc::TC - 1) / tc::TC;
+    int best_mt = 0;
     double best_eff = 0;
-    const int cands[] = {W, 126, 128, 62, 64};
-    for (int TC : cands) {
-        // TMA boxes are at most 256 elements per dimension
-        if (TC < 1 || TC > W || TC + K - 1 > 256) continue;
-        const int WP = TC + K - 1;
-        for (int TR = 1; TR <= H && TR + K - 1 <= 256 && TR <= 64; ++TR) {
-            const int MT = (TR * WP + 127) / 128;
-            if (MT * N > tc::TMEM_BUF) break;
-            const int P = tc_plane_pixels(MT, K, WP);
-            const size_t total = w_bytes + tc::NSTAGE * (2 * (size_t)P * 16);
-            if (total > 220 * 1024) break;
-            const long long tiles = (long long)((W + TC - 1) / TC) * ((H + TR - 1) / TR) * Nimg;
-            // useful fraction of MMA rows, of the tile area, and of the persistent grid
-            const double rows = (double)TR * TC / ((double)MT * 128);
-            const double edge = (double)W * H / ((double)((W + TC - 1) / TC) * TC * ((H + TR - 1) / TR) * TR);
-            const int sms = (device_sm_count() + groups - 1) / groups;  // SMs per channel group
-            const long long rounds = (tiles + sms - 1) / sms;
-            const double fill = (double)tiles / ((double)rounds * sms);
-            // each tile re-reads K - 1 halo rows of input
-            const double halo = (double)TR / (TR + K - 1);
-            const double eff = rows * edge * fill * halo;
-            if (eff > best_eff + 1e-9) {
-                best_eff = eff;
-                best_tc = TC;
-                best_tr = TR;
-            }
+    // the OIHW weights are staged in the stage buffers first: an odd pitch
+    // of 16-byte units per output channel
+    const int raw_pitch = (Cin * RS / 4) | 1;
+    const size_t raw = (size_t)Cg * raw_pitch * 16;
+    for (int MT = 1; MT * NB <= tc::TMEM_BUF && MT <= 16; ++MT) {
+        const int TR = 4 * MT;
+        const size_t stage = (size_t)(TR + 2) * tc::WP * tc::CH * 4;
+        if (fixed + tc::MIN_STAGE * stage > kTcSmemCap) break;
+        const size_t nfit = (kTcSmemCap - fixed) / stage;
+        if ((nfit < tc::MAX_STAGE ? nfit : tc::MAX_STAGE) * stage < raw) continue;
+        const long long tiles = (long long)tiles_x * ((H + TR - 1) / TR) * Nimg;
+        const long long rounds = (tiles + sms - 1) / sms;
+        const double fill = (double)tiles / ((double)rounds * sms);
+        const double edge = (double)H / ((double)((H + TR - 1) / TR) * TR);
+        const double halo = (double)TR / (TR + 2);
+        const double eff = fill * edge * halo;
+        if (eff > best_eff + 1e-9) {
+            best_eff = eff;
+            best_mt = MT;
         }
     }
-    if (best_tc < 0) return false;
-    g.TC = best_tc;
-    g.TR = best_tr;
-    g.WP = g.TC + K - 1;
-    g.THh = g.TR + K - 1;
-    g.MT = (g.TR * g.WP + 127) / 128;
-    g.P = tc_plane_pixels(g.MT, K, g.WP);
-    g.tiles_x = (W + g.TC - 1) / g.TC;
+    if (best_mt == 0) return false;
+    g.MT = best_mt;
+    g.TR = 4 * g.MT;
+    g.THh = g.TR + 2;
+    g.tiles_x = tiles_x;
     g.tiles_y = (H + g.TR - 1) / g.TR;
     g.ntiles = g.tiles_x * g.tiles_y * Nimg;
     g.nk = nk;
-    g.a_plane_bytes = (uint32_t)g.P * 16;
-    g.a_bytes = 2 * g.a_plane_bytes;
-    g.box_bytes = (uint32_t)(4 * g.WP * g.THh * 4);
-    g.w_bytes = (uint32_t)((w_bytes + 1023) & ~(size_t)1023);
-    g.smem_bytes = g.w_bytes + tc::NSTAGE * g.a_bytes;
+    g.nstg = (Cin + tc::CH - 1) / tc::CH;
+    g.stage_bytes = (uint32_t)((size_t)g.THh * tc::WP * tc::CH * 4);
+    g.w_bytes = (uint32_t)w_bytes;
+    const int ns = (int)((kTcSmemCap - fixed) / g.stage_bytes);
+    g.nstage = ns < tc::MAX_STAGE ? ns : tc::MAX_STAGE;
+    g.raw_pitch = raw_pitch;
+    g.smem_bytes = (uint32_t)(fixed + (size_t)g.nstage * g.stage_bytes);
     g.tmem_cols = 2 * tc::TMEM_BUF;
     return true;
 }
@@ -424,55 +610,74 @@ static PFN_cuTensorMapEncodeTiled_v12000 tc_tensor_map_encoder()
     return fn;
 }
 
-template <int K, int N>
-static cudaError_t launch_tc_n(const ConvArgs &a, cudaStream_t st)
+template <int CG>
+static cudaError_t launch_tc_cg(const ConvArgs &a, cudaStream_t st)
 {
+    constexpr int NB = (3 * CG + 15) / 16 * 16;
     tc::TcGeom g;
-    const int groups = (a.Cout + N - 1) / N;
-    if (!tc_geometry(K, N, groups, a.Cin, a.H, a.W, a.N, g)) return cudaErrorNotSupported;
+    const int groups = (a.Cout + CG - 1) / CG;
+    if (!tc_geometry(CG, NB, groups, a.Cin, a.R * a.S, a.H, a.W, a.N, g)) return cudaErrorNotSupported;
     if ((long long)g.tiles_x * g.tiles_y * a.N > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     PFN_cuTensorMapEncodeTiled_v12000 encode = tc_tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
-    // NHWC activations as a 4-D tensor (C, W, H, N); box = one 4-channel block
-    // of the tile's padded pixels
+    // NHWC activations as a 4-D tensor (C, W, H, N); box = 32 channels (one
+    // 128-byte swizzled row per pixel; channels past Cin read as zero) x 32
+    // padded columns x (TR + 2) rows of one image
     CUtensorMap tm;
     const cuuint64_t dims[4] = {(cuuint64_t)a.Cin, (cuuint64_t)a.W, (cuuint64_t)a.H, (cuuint64_t)a.N};
     const cuuint64_t strides[3] = {(cuuint64_t)a.Cin * 4, (cuuint64_t)a.W * a.Cin * 4,
                                    (cuuint64_t)a.H * a.W * a.Cin * 4};
-    const cuuint32_t box[4] = {4, (cuuint32_t)g.WP, (cuuint32_t)g.THh, 1};
+    const cuuint32_t box[4] = {(cuuint32_t)tc::CH, (cuuint32_t)tc::WP, (cuuint32_t)g.THh, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     if (encode(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(a.x), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorNotSupported;
+    // NHWC output as (C, W, H, N); box = the group's CG channels x TC pixels
+    // of one row, swizzled like the epilogue's buffers (groups of 16 or 32
+    // channels; smaller groups store directly and leave this map unused)
+    CUtensorMap tmo;
+    std::memset(&tmo, 0, sizeof(tmo));
+    if (CG >= 16) {
+        const cuuint64_t odims[4] = {(cuuint64_t)a.Cout, (cuuint64_t)a.W, (cuuint64_t)a.H, (cuuint64_t)a.N};
+        const cuuint64_t ostrides[3] = {(cuuint64_t)a.Cout * 4, (cuuint64_t)a.W * a.Cout * 4,
+                                        (cuuint64_t)a.H * a.W * a.Cout * 4};
+        const cuuint32_t obox[4] = {(cuuint32_t)CG, (cuuint32_t)tc::TC, 1, 1};
+        if (encode(&tmo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.y, odims, ostrides, obox, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CG == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorNotSupported;
+    }
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     static int allowed[64] = {0};
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (allowed[dev] < (int)g.smem_bytes) {
-        e = cudaFuncSetAttribute(conv_tc_kernel<K, N>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem_bytes);
+        e = cudaFuncSetAttribute(conv_tc_kernel<CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem_bytes);
         if (e != cudaSuccess) return e;
         allowed[dev] = (int)g.smem_bytes;
     }
-    const int per_group = (device_sm_count() + groups - 1) / groups;
+    const int per_group = device_sm_count() / groups > 0 ? device_sm_count() / groups : 1;
     const int grid = g.ntiles < per_group ? g.ntiles : per_group;
-    conv_tc_kernel<K, N><<<dim3(grid, groups), tc::NTHREADS, g.smem_bytes, st>>>(
-        tm, a.w, a.b, a.y, a.N, a.H, a.W, a.Cin, a.Cout, a.R, a.S, a.act, g, device_status_ptr(), 1000000000ull);
+    conv_tc_kernel<CG><<<dim3(grid, groups), tc::NTHREADS, g.smem_bytes, st>>>(
+        tm, tmo, a.w, a.b, a.y, a.H, a.W, a.Cin, a.Cout, a.R, a.S, a.act, g, device_status_ptr(), 1000000000ull);
     return cudaGetLastError();
 }
 
 cudaError_t launch_conv_tc(const ConvArgs &a, cudaStream_t st)
 {
     if (a.R > 3 || a.S > 3) return cudaErrorNotSupported;
-    // up to 64 output channels per CTA; more run as groups of 64
-    const int n16 = (a.Cout + 15) / 16 * 16;
-    switch (n16) {
-    case 16: return launch_tc_n<3, 16>(a, st);
-    case 32: return launch_tc_n<3, 32>(a, st);
-    case 48: return launch_tc_n<3, 48>(a, st);
-    default: return launch_tc_n<3, 64>(a, st);
-    }
+    // output channels per CTA: the smallest group that holds Cout, at most 32
+    // (larger Cout runs as groups on blockIdx.y); where a group's filters do
+    // not fit in shared memory, smaller groups (a smaller MMA N, lower
+    // tensor-core efficiency)
+    cudaError_t e = cudaErrorNotSupported;
+    if (a.Cout > 16) e = launch_tc_cg<32>(a, st);
+    if (e == cudaErrorNotSupported && a.Cout > 8) e = launch_tc_cg<16>(a, st);
+    if (e == cudaErrorNotSupported && a.Cout > 4) e = launch_tc_cg<8>(a, st);
+    if (e == cudaErrorNotSupported) e = launch_tc_cg<4>(a, st);
+    return e;
 }
 
 }  // namespace sc

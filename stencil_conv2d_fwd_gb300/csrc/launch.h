@@ -49,6 +49,11 @@ cudaError_t launch_ffma_peak(float *sink, int blocks, int iters, cudaStream_t st
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
+// Stream-ordered temporary buffers (api.cu) from a library-private memory
+// pool of the current device; see sc_release_workspace.
+cudaError_t workspace_alloc(void **p, size_t bytes, cudaStream_t st);
+cudaError_t workspace_free(void *p, cudaStream_t st);
+
 // Device address of the current device's status word (api.cu), or nullptr.
 int *device_status_ptr();
 

@@ -40,6 +40,9 @@ SHAPES = [
     (1, 16, 48, 11, 257, 3, 3),
     (1, 8, 16, 12, 17, 1, 1),
     (1, 8, 12, 12, 17, 3, 1),
+    # filters too large for 32-channel groups: 16- and 8-channel groups
+    (1, 128, 32, 9, 40, 3, 3),
+    (1, 256, 12, 6, 33, 3, 3),
 ]
 
 
@@ -70,3 +73,12 @@ def test_tc_rejects_what_it_does_not_run(cuda_dev, sc):
     y = torch.zeros(4 * 8 * 8 * 4, device=cuda_dev)
     assert sc.conv2d_fwd_tc(x, w, None, y, 1, 8, 8, 6, 4, 3, 3, 0) == sc.SC_ERR_UNSUPPORTED
     assert sc.conv2d_fwd_tc(x, w, None, y, 1, 8, 8, 4, 4, 5, 5, 0) == sc.SC_ERR_UNSUPPORTED
+    # filters that stay too large even in 4-channel groups
+    xb = torch.zeros(8 * 8 * 600, device=cuda_dev)
+    wb = torch.zeros(4 * 600 * 9, device=cuda_dev)
+    assert sc.conv2d_fwd_tc(xb, wb, None, y, 1, 8, 8, 600, 4, 3, 3, 0) == sc.SC_ERR_UNSUPPORTED
+    # the filters are bulk-copied: w must be 16-byte aligned like x and y
+    wu = torch.zeros(4 * 4 * 9 + 1, device=cuda_dev)[1:]
+    assert sc.conv2d_fwd_tc(x, wu, None, y, 1, 8, 8, 4, 4, 3, 3, 0) == sc.SC_ERR_ALIGN
+    torch.cuda.synchronize()
+    assert sc.sc_last_device_status() == sc.SC_OK
