@@ -42,7 +42,7 @@ FP32_LANES_PER_SM = 128          # FP32 FMA lanes per Blackwell SM (4 schedulers
 # --only cases: (workload id, layer index; None = the stencil pipeline)
 ONLY_CASES = {
     "1": (1, 0), "2": (2, 0), "3-L1": (3, 0), "3-L2": (3, 1), "3-L3": (3, 2), "4": (4, 0), "5": (5, None),
-    "4-tc": (4, 0), "3-L2-tc": (3, 1),
+    "4-tc": (4, 0), "3-L2-tc": (3, 1), "3-L3-tc": (3, 2),
 }
 
 

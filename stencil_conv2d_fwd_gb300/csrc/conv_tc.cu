@@ -378,11 +378,24 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
             const uint32_t a_lbo = 1u << 16, b_lbo = (uint32_t)NB << 16;
             // G M-tiles at a time, M-tiles innermost: consecutive MMAs go to
             // different accumulators (back-to-back MMAs into one accumulator
-            // issue more slowly).  A: +2 units (32 B) per K step, +256 units
+            // issue more slowly); a full stage (4 K steps) is unrolled so that
+            // every descriptor is a register plus a constant.  A: +2 units (32 B) per K step, +256 units
             // (4 KB) per vertical tap, +1024 units (16 KB) per M-tile.  B:
             // 2 * NB units per (K step, tap).
             auto issue = [&](auto gsz, uint32_t d0, uint32_t a0, uint32_t b0, int nks, uint32_t acc0) {
                 constexpr int G = decltype(gsz)::value;
+                if (nks == 4) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                        for (int r = 0; r < 3; ++r)
+#pragma unroll
+                            for (int gi = 0; gi < G; ++gi)
+                                tc::mma_tf32_w(d0 + (uint32_t)(gi * NB), a0 + (uint32_t)(kk * 2 + r * 256 + gi * 1024),
+                                               tc::A_HI, b0 + (uint32_t)((kk * 3 + r) * 2 * NB), tc::B_HI, idesc,
+                                               (kk > 0 || r > 0) ? 1u : acc0);
+                    return;
+                }
 #pragma unroll 1
                 for (int kk = 0; kk < nks; ++kk) {
 #pragma unroll
