@@ -43,6 +43,7 @@ FP32_LANES_PER_SM = 128          # FP32 FMA lanes per Blackwell SM (4 schedulers
 ONLY_CASES = {
     "1": (1, 0), "2": (2, 0), "3-L1": (3, 0), "3-L2": (3, 1), "3-L3": (3, 2), "4": (4, 0), "5": (5, None),
     "4-tc": (4, 0), "3-L2-tc": (3, 1), "3-L3-tc": (3, 2),
+    "4-bf16": (4, 0), "3-L2-bf16": (3, 1), "3-L3-bf16": (3, 2),
 }
 
 
@@ -460,6 +461,38 @@ def per_config(sc, S, dev, stream, flush, fp32_tflops, hbm_gbs, hbm_src):
                      "tolerance": "5e-3 * sum|x*w| (TF32 operands)",
                      "tf32_peak_tflops": round(tf32_tflops, 1)}
 
+    # bf16 activation storage with BF16 tensor-core operands (conv2d_fwd_tc_bf16):
+    # x and y bf16 in HBM (the synthetic input rounded to bf16), fp32 filters and
+    # bias; roofline against the measured BF16 peak and HBM
+    bf16_tflops = float(peaks.get("bf16_tflops", 1900.0))
+    for name, cid, li in (("4 (tcgen05 BF16, bf16 x/y)", 4, 0), ("3-L2 (tcgen05 BF16, bf16 x/y)", 3, 1),
+                          ("3-L3 (tcgen05 BF16, bf16 x/y)", 3, 2)):
+        wl = S.config(cid)
+        L = wl.layers[li]
+        xin = wl.x if li == 0 else np.maximum(S.uniform(77, 0, (wl.n, L.cin, wl.h, wl.w), -1, 1), 0)
+        xd = torch.from_numpy(np.ascontiguousarray(xin.transpose(0, 2, 3, 1)).astype(np.float32)).to(dev)
+        xd = xd.to(torch.bfloat16)
+        wd, bd = torch.from_numpy(L.w).to(dev), torch.from_numpy(L.b).to(dev)
+        yd = torch.empty(wl.n * wl.h * wl.w * L.cout, dtype=torch.bfloat16, device=dev)
+
+        def call_bf(s=None):
+            rc = sc.conv2d_fwd_tc_bf16(xd, wd, bd, yd, wl.n, wl.h, wl.w, L.cin, L.cout, L.r, L.s, L.act,
+                                       sc.SC_BF16, s if s is not None else stream)
+            if rc != 0:
+                raise RuntimeError(sc.sc_status_string(rc))
+        med, mn = time_events(call_bf, stream, flush, reps=20)
+        flops = conv_flops(wl.n, wl.h, wl.w, L)
+        byts = 2 * wl.n * wl.h * wl.w * (L.cin + L.cout) + 4 * (L.w.size + L.b.size)
+        t_c, t_m = flops / (bf16_tflops * 1e12), byts / (hbm_gbs * 1e9)
+        out[name] = {"ms_median": round(med, 5), "ms_min": round(mn, 5),
+                     "gflops": round(flops / (med * 1e-3) / 1e9, 2),
+                     "mpixel_per_s": round(wl.n * wl.h * wl.w / (med * 1e-3) / 1e6, 2),
+                     "roofline_bound": "tensor" if t_c >= t_m else "hbm",
+                     "roofline_us": round(max(t_c, t_m) * 1e6, 3),
+                     "roofline_frac": round(max(t_c, t_m) / (med * 1e-3), 4),
+                     "tolerance": "5e-3 * sum|x*w| + 2^-8 |y| (bf16 operands and storage)",
+                     "bf16_peak_tflops": round(bf16_tflops, 1)}
+
     c5 = S.config(5)
     ind = torch.from_numpy(c5.img).to(dev)
     outd = torch.empty_like(ind)
@@ -596,6 +629,11 @@ def run_only(args, local):
                 x = y
         if args.only.endswith("-tc"):   # the tensor-core (TF32) variant
             launch = lambda: sc.conv2d_fwd_tc(x, wd, bd, y, N, H, W, L.cin, L.cout, L.r, L.s, L.act)
+        elif args.only.endswith("-bf16"):   # bf16 storage, BF16 tensor-core operands
+            xb = x.to(torch.bfloat16)
+            yb = torch.empty(N * H * W * L.cout, dtype=torch.bfloat16, device=dev)
+            launch = lambda: sc.conv2d_fwd_tc_bf16(xb, wd, bd, yb, N, H, W, L.cin, L.cout, L.r, L.s, L.act,
+                                                   sc.SC_BF16)
         else:
             launch = lambda: sc.conv2d_fwd(x, wd, bd, y, N, H, W, L.cin, L.cout, L.r, L.s, sc.SC_NHWC, L.act)
     for _ in range(args.warmup + args.steps):

@@ -38,6 +38,7 @@ typedef enum {
 
 typedef enum { SC_NCHW = 0, SC_NHWC = 1 } sc_layout;
 typedef enum { SC_ACT_NONE = 0, SC_ACT_RELU = 1 } sc_act;
+typedef enum { SC_F32 = 0, SC_BF16 = 1 } sc_dtype;   /* element type of an activation tensor */
 
 /*
  * conv2d_fwd: y = act(conv(x, w) + b), stride 1, zero "same" padding.
@@ -91,6 +92,29 @@ int conv2d_fwd(const float *x, const float *w, const float *b, float *y,
 int conv2d_fwd_tc(const float *x, const float *w, const float *b, float *y,
                   int N, int H, int W, int Cin, int Cout, int R, int S,
                   int act, sc_stream_t stream);
+
+/*
+ * conv2d_fwd_tc_bf16: conv2d_fwd_tc with bf16 activation storage and BF16
+ * tensor-core operands (tcgen05 kind::f16), fp32 accumulation.  Storing
+ * activations in 16-bit floats halves their bytes ("Optimizing convolution
+ * kernels - CNNs in Vulkan Part 2/3", the fp16 storage section: the traffic
+ * halves at a small loss of precision).  x is bf16, the filters are fp32 and
+ * rounded to bf16 (to nearest even) inside, b is fp32, y is bf16 (rounded to
+ * nearest even) or fp32.  With x exact in bf16 (8 significant bits, unit
+ * roundoff 2^-8), |y - y_ref| <= 2^-8 * sum|x*w| (weight rounding) + fp32
+ * accumulation error, within 5e-3 * (sum |x * w| + |b|); a bf16 y adds its
+ * own rounding, at most 2^-8 * |y_ref|.
+ * x : N*H*W*Cin bf16 (NHWC), 16-byte aligned.  y : N*H*W*Cout elements of
+ *   y_dtype (SC_F32 or SC_BF16), NHWC, 16-byte aligned.  w : OIHW fp32,
+ *   16-byte aligned.  b : Cout floats or NULL.
+ * Supported: Cin % 8 == 0, Cout % 4 == 0, Cout <= 128 (bf16 y with
+ *   Cout > 16: Cout % 8 == 0), R and S odd and <= 3, filters that fit in
+ *   shared memory as for conv2d_fwd_tc.
+ * Returns SC_OK or a negative sc_status.
+ */
+int conv2d_fwd_tc_bf16(const void *x, const float *w, const float *b, void *y,
+                       int N, int H, int W, int Cin, int Cout, int R, int S,
+                       int act, int y_dtype, sc_stream_t stream);
 
 /*
  * stencil_pipeline_fwd: three stencil stages fused in one pass over a

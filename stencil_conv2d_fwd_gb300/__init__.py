@@ -30,6 +30,8 @@ SC_NCHW = 0
 SC_NHWC = 1
 SC_ACT_NONE = 0
 SC_ACT_RELU = 1
+SC_F32 = 0
+SC_BF16 = 1
 
 # Every symbol include/stencilconv.h declares, with (restype, argtypes).
 _P = ctypes.c_void_p
@@ -37,6 +39,7 @@ _I = ctypes.c_int
 SIGNATURES = {
     "conv2d_fwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "conv2d_fwd_tc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
+    "conv2d_fwd_tc_bf16": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "stencil_pipeline_fwd": (_I, [_P, _P, _I, _I, _P]),
     "sc_repack": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "sc_last_device_status": (_I, [_P]),
@@ -108,6 +111,13 @@ def conv2d_fwd_tc(x, w, b, y, N, H, W, Cin, Cout, R, S, act=SC_ACT_NONE, stream=
     """Tensor-core (TF32) variant of conv2d_fwd, NHWC only (see the header)."""
     return load().conv2d_fwd_tc(_ptr(x), _ptr(w), _ptr(b), _ptr(y), N, H, W, Cin, Cout, R, S, act,
                                 _stream(stream))
+
+
+def conv2d_fwd_tc_bf16(x, w, b, y, N, H, W, Cin, Cout, R, S, act=SC_ACT_NONE, y_dtype=SC_BF16,
+                       stream=None) -> int:
+    """BF16-storage tensor-core variant: x bf16, y bf16 or fp32 (see the header)."""
+    return load().conv2d_fwd_tc_bf16(_ptr(x), _ptr(w), _ptr(b), _ptr(y), N, H, W, Cin, Cout, R, S, act, y_dtype,
+                                     _stream(stream))
 
 
 def stencil_pipeline_fwd(inp, out, H, W, stream=None) -> int:

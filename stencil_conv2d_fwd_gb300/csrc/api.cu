@@ -233,6 +233,32 @@ int conv2d_fwd_tc(const float *x, const float *w, const float *b, float *y, int 
     return e == cudaSuccess ? SC_OK : cuda_fail(e);
 }
 
+int conv2d_fwd_tc_bf16(const void *x, const float *w, const float *b, void *y, int N, int H, int W, int Cin,
+                       int Cout, int R, int S, int act, int y_dtype, sc_stream_t stream)
+{
+    if (!x || !w || !y) return SC_ERR_NULL;
+    const long long nx = checked_count({N, H, W, Cin});
+    const long long ny = checked_count({N, H, W, Cout});
+    const long long nw = checked_count({Cout, Cin, R, S});
+    if (nx < 0 || ny < 0 || nw < 0) return SC_ERR_SHAPE;
+    if (H > (1 << 30) || W > (1 << 30)) return SC_ERR_SHAPE;
+    if ((R & 1) == 0 || (S & 1) == 0 || R > 3 || S > 3) return SC_ERR_UNSUPPORTED;
+    if (act != SC_ACT_NONE && act != SC_ACT_RELU) return SC_ERR_UNSUPPORTED;
+    if (y_dtype != SC_F32 && y_dtype != SC_BF16) return SC_ERR_UNSUPPORTED;
+    if ((Cin % 8) != 0 || (Cout % 4) != 0 || Cout > 128) return SC_ERR_UNSUPPORTED;
+    if (y_dtype == SC_BF16 && Cout > 16 && (Cout % 8) != 0) return SC_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(y) || !aligned16(w)) return SC_ERR_ALIGN;
+    const size_t ybytes = (size_t)ny * (y_dtype == SC_BF16 ? 2 : 4);
+    if (overlaps(y, ybytes, x, (size_t)nx * 2) || overlaps(y, ybytes, w, (size_t)nw * sizeof(float)) ||
+        overlaps(y, ybytes, b, b ? (size_t)Cout * sizeof(float) : 0))
+        return SC_ERR_ALIAS;
+    // the bf16 tensors travel in ConvArgs' pointer fields; only the kernels read them
+    sc::ConvArgs a{static_cast<const float *>(x), w, b, static_cast<float *>(y), N, H, W, Cin, Cout, R, S, act};
+    const cudaError_t e = sc::launch_conv_tc_bf16(a, y_dtype == SC_BF16, reinterpret_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return SC_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? SC_OK : cuda_fail(e);
+}
+
 int stencil_pipeline_fwd(const float *in, float *out, int H, int W, sc_stream_t stream)
 {
     if (!in || !out) return SC_ERR_NULL;

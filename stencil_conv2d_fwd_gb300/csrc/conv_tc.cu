@@ -64,6 +64,7 @@
 // memory and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 
 #include <cstring>
 #include <mutex>
@@ -76,21 +77,44 @@ namespace sc {
 
 namespace tc {
 
-constexpr int NTHREADS = 192;   // warps 0-3 epilogue (TMEM lane quadrants), 4 producer, 5 MMA
+constexpr int NTHREADS = 320;   // warps 4 producer, 5 MMA; 0-3 and 6-9 epilogue (two sets, TMEM lane quadrant = warp % 4)
 constexpr int WP = 32;          // padded row pitch (pixels) = lanes of a warp
 constexpr int TC = 30;          // output columns per tile
-constexpr int CH = 32;          // channels per stage (one 128-byte swizzled row per pixel)
+constexpr int CH = 32;          // channels per stage (one swizzled row per pixel)
 constexpr int MIN_STAGE = 2;
 constexpr int MAX_STAGE = 6;
 constexpr int TMEM_BUF = 256;   // tensor-memory columns per accumulator buffer (two buffers)
 constexpr int OUT_BUF = 4096;                // one epilogue output buffer: 30 pixel rows of up to 128 bytes
-constexpr int STG_BYTES = 4 * 2 * OUT_BUF;   // two per epilogue warp
+constexpr int STG_BYTES = 8 * OUT_BUF;       // one per epilogue warp
 
-// Instruction descriptor, kind::tf32: D = F32, A = B = TF32, both K-major,
-// dense, M = 128.
-__host__ __device__ constexpr uint32_t idesc_tf32(int n)
+// Operand kinds.  Either way a K step (one MMA's K) is 32 bytes of a pixel's
+// channels and one 16-byte chunk of a B row holds CU = KC / 2 channels.  A
+// 32-channel stage is SUB sub-buffers, each filled by one TMA box, with one
+// ROWB-byte swizzled row per padded pixel.  The row widths are chosen so that
+// the tensor core's read of a 32-byte K slice of 8 consecutive rows touches
+// every 16-byte bank group exactly twice (no conflicts): 128-byte rows with
+// 128-byte swizzling, or 32-byte rows with 32-byte swizzling (64-byte rows
+// with 64-byte swizzling would put rows r and r + 2 on the same banks).
+//  * OpTF32: fp32 activations, TF32 MMA (kind::tf32), K step = 8 channels;
+//    one 128-byte row of 32 channels per pixel (4 K steps per row).
+//  * OpBF16: bf16 activations, BF16 MMA (kind::f16), K step = 16 channels;
+//    two sub-buffers of 32-byte rows (16 channels, one K step each).  The
+//    fp32 filters are rounded to bf16 (to nearest even) when the CTA stages
+//    them.
+struct OpTF32 {
+    static constexpr int ESZ = 4, KC = 8, ROWB = 128, SUB = 1;
+    static constexpr uint32_t A_LAYOUT = 2, FMT = 2;   // descriptor layout 128B swizzle; TF32
+};
+struct OpBF16 {
+    static constexpr int ESZ = 2, KC = 16, ROWB = 32, SUB = 2;
+    static constexpr uint32_t A_LAYOUT = 6, FMT = 1;   // descriptor layout 32B swizzle; BF16
+};
+
+// Instruction descriptor: D = F32, A = B = FMT (TF32 2, BF16 1), both
+// K-major, dense, M = 128.
+__host__ __device__ constexpr uint32_t idesc_mma(uint32_t fmt, int n)
 {
-    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n >> 3) << 17) | ((128u >> 4) << 24);
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(n >> 3) << 17) | ((128u >> 4) << 24);
 }
 
 // Shared-memory matrix descriptors as two 32-bit words: low = start address
@@ -99,23 +123,46 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int n)
 // descriptor; 0 = no swizzle, 2 = 128-byte swizzle); base offset 0.  Shared
 // addresses stay below 2^18, so stepping a start address is one 32-bit add
 // that cannot carry into the LBO field.
-constexpr uint32_t A_HI = (1024u >> 4) | (1u << 14) | (2u << 29);
+template <class OP>
+__host__ __device__ constexpr uint32_t a_hi() { return ((8u * OP::ROWB) >> 4) | (1u << 14) | (OP::A_LAYOUT << 29); }   // SBO = 8 rows
 constexpr uint32_t B_HI = (128u >> 4) | (1u << 14);
 
-__device__ __forceinline__ void mma_tf32_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo, uint32_t b_hi,
-                                           uint32_t idesc, uint32_t acc)
+template <class OP>
+__device__ __forceinline__ void mma_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo, uint32_t b_hi,
+                                      uint32_t idesc, uint32_t acc)
 {
-    asm volatile(
-        "{\n"
-        ".reg .pred p;\n"
-        ".reg .b64 da, db;\n"
-        "setp.ne.b32 p, %6, 0;\n"
-        "mov.b64 da, {%1, %2};\n"
-        "mov.b64 db, {%3, %4};\n"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], da, db, %5, p;\n"
-        "}\n" ::"r"(d_tmem),
-        "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc)
-        : "memory");
+    if constexpr (OP::FMT == 2) {
+        asm volatile(
+            "{\n"
+            ".reg .pred p;\n"
+            ".reg .b64 da, db;\n"
+            "setp.ne.b32 p, %6, 0;\n"
+            "mov.b64 da, {%1, %2};\n"
+            "mov.b64 db, {%3, %4};\n"
+            "tcgen05.mma.cta_group::1.kind::tf32 [%0], da, db, %5, p;\n"
+            "}\n" ::"r"(d_tmem),
+            "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n"
+            ".reg .pred p;\n"
+            ".reg .b64 da, db;\n"
+            "setp.ne.b32 p, %6, 0;\n"
+            "mov.b64 da, {%1, %2};\n"
+            "mov.b64 db, {%3, %4};\n"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n"
+            "}\n" ::"r"(d_tmem),
+            "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc)
+            : "memory");
+    }
+}
+
+// Two floats -> two bf16 (round to nearest even), `lo` at the lower address.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
+{
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar)
@@ -173,27 +220,27 @@ __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[CW])
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d)
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
 {
-    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-// Swizzle key of pixel row p of an epilogue output buffer (rows of CW
-// floats, 1024-byte aligned): 16-byte chunk q of row p is stored at chunk
-// q ^ key(p).  This is the TMA's own 128-byte (CW = 32) or 64-byte (CW = 16)
-// swizzle pattern, so the buffer is a valid source for a swizzled TMA store,
-// and the row-wise writes (one row per lane) of every 8-lane phase touch 8
-// distinct 16-byte bank groups.
-template <int CW>
+// Swizzle key of pixel row p of an epilogue output buffer (rows of ROWB =
+// 128 or 64 bytes, 1024-byte aligned): 16-byte chunk q of row p is stored at
+// chunk q ^ key(p).  This is the TMA's own 128-byte or 64-byte swizzle
+// pattern, so the buffer is a valid source for a swizzled TMA store, and the
+// row-wise writes (one row per lane) of every 8-lane phase touch 8 distinct
+// 16-byte bank groups.
+template <int ROWB>
 __device__ __forceinline__ int stg_key(int p)
 {
-    return CW == 32 ? (p & 7) : ((p >> 1) & 3);
+    return ROWB == 128 ? (p & 7) : ((p >> 1) & 3);
 }
 
 struct TcGeom {
     int MT, TR, THh;                // M-tiles per tile, tile rows (4 * MT), staged rows (TR + 2)
     int tiles_x, tiles_y, ntiles;   // tiles of TC x TR output pixels, per image and in all
-    int nk, nstg, nstage;           // 8-channel K steps, 32-channel stages per tile, stage buffers
+    int nk, nstg, nstage;           // K steps, 32-channel stages per tile, stage buffers
     int raw_pitch;                  // 16-byte units per output channel of the staged OIHW filters
     uint32_t stage_bytes, w_bytes, smem_bytes, tmem_cols;
 };
@@ -203,17 +250,23 @@ struct TcGeom {
 __device__ __forceinline__ void give_up_flag(int &flag) { atomicExch(&flag, 1); }
 
 // CG: output channels per CTA (4, 8, 16 or 32); NB = MMA N = 3 * CG rounded
-// up to 16.
-template <int CG>
+// up to 16.  OP: operand kind (tc::OpTF32, tc::OpBF16).  YBF16: y is bf16
+// (else fp32).
+template <int CG, class OP, bool YBF16>
 __global__ void __launch_bounds__(tc::NTHREADS, 1)
     conv_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmy,
-                   const float *__restrict__ w, const float *__restrict__ bias, float *__restrict__ y, int H, int W,
+                   const float *__restrict__ w, const float *__restrict__ bias, void *__restrict__ yv, int H, int W,
                    int Cin, int Cout, int R, int S, int act, tc::TcGeom g, int *status, unsigned long long timeout_ns)
 {
     constexpr int NB = (3 * CG + 15) / 16 * 16;
+    constexpr int KS = tc::CH / OP::KC;            // K steps per stage
+    constexpr int KSUB = KS / OP::SUB;             // K steps per sub-buffer
+    constexpr int CU = OP::KC / 2;                 // input channels per 16-byte B chunk
     constexpr int CW = CG;                         // epilogue column chunk = the group
-    constexpr bool TMA_OUT = CW >= 16;             // store through a shared-memory buffer and TMA
-    constexpr int CPR = CW / 4;                    // 16-byte chunks per pixel
+    constexpr int OSZ = YBF16 ? 2 : 4;             // bytes per output element
+    constexpr int OROWB = CW * OSZ;                // bytes of one pixel's group of outputs
+    constexpr bool TMA_OUT = OROWB >= 64;          // store through a swizzled shared-memory buffer and TMA
+    constexpr int OCH = OROWB >= 16 ? OROWB / 16 : 1;   // 16-byte chunks per pixel (or one 8-byte piece)
     extern __shared__ __align__(1024) unsigned char smem_dyn[];
     __shared__ __align__(8) unsigned long long full_bar[tc::MAX_STAGE], empty_bar[tc::MAX_STAGE];
     __shared__ __align__(8) unsigned long long acc_full[2], acc_empty[2], w_bar, wt_bar;
@@ -234,13 +287,14 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
     // weights (one contiguous run of Cin * R * S floats per output channel)
     // into the top of the stage buffers, rows g.raw_pitch 16-byte units apart
     // (an odd number, so that the 16-byte reads below are free of bank
-    // conflicts); warps 0-3 and 5 then rearrange them into the MMA's B
-    // layout: the [k][r][cb][n][4] bank whose element (k, r, cb, n, j) with
-    // n = s * CG + co is w[co0 + co][8k + 4cb + j][r - (3 - R) / 2][s - (3 - S) / 2],
-    // zero for n >= 3 * CG, taps the R x S filter lacks, channels beyond Cin
-    // and co beyond Cout.  One unit is one output channel and one block of 4
-    // input channels; neighbouring lanes take neighbouring output channels,
-    // whose B rows are neighbours.  Meanwhile the producer already fills the
+    // conflicts); the other warps then rearrange them into the MMA's B
+    // layout: the [k][r][cb][n][CU] bank whose element (k, r, cb, n, j) with
+    // n = s * CG + co is w[co0 + co][KC k + CU cb + j][r - (3 - R) / 2][s - (3 - S) / 2]
+    // (as TF32 or rounded to bf16), zero for n >= 3 * CG, taps the R x S
+    // filter lacks, channels beyond Cin and co beyond Cout.  One unit is one
+    // output channel and one block of CU input channels (one 16-byte chunk);
+    // neighbouring lanes take neighbouring output channels, whose B rows are
+    // neighbours.  Meanwhile the producer already fills the
     // stage buffers below the staged weights; `wt_bar` (one arrive per
     // rearranging warp) releases the rest, and the bank, to the MMA warp.
     const int RS = R * S;
@@ -255,10 +309,10 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
         }
         for (int j = 0; j < 2; ++j) {
             mbar_init(smem_u32(&acc_full[j]), 1);
-            mbar_init(smem_u32(&acc_empty[j]), 4);   // one arrive per epilogue warp
+            mbar_init(smem_u32(&acc_empty[j]), 8);   // one arrive per epilogue warp
         }
         mbar_init(smem_u32(&w_bar), 1);
-        mbar_init(smem_u32(&wt_bar), 5);
+        mbar_init(smem_u32(&wt_bar), tc::NTHREADS / 32 - 1);   // every warp but the producer
         abort_sh = 0;
         fence_mbar_init();
     }
@@ -277,20 +331,20 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
         const bool landed = mbar_wait_bounded(smem_u32(&w_bar), 0, timeout_ns);
         if (!landed) give_up_flag(abort_sh);
         const float *raw = reinterpret_cast<const float *>(raw_sm);
-        float4 *bank = reinterpret_cast<float4 *>(wsm);
-        constexpr int LT = tc::NTHREADS - 32;   // threads of warps 0-3 and 5
+        uint4 *bank = reinterpret_cast<uint4 *>(wsm);
+        constexpr int LT = tc::NTHREADS - 32;   // threads of every warp but the producer
         const int lt = warp < 4 ? tid : tid - 32;
         const int units = CG * 2 * g.nk;
         for (int u = lt; landed && u < units; u += LT) {
             const int co = u % CG, cib = u / CG;
-            const int k = cib >> 1, cb = cib & 1;
-            const bool ok = co < co_n && 4 * cib < Cin;
-            const float *src = raw + (size_t)co * g.raw_pitch * 4 + (size_t)4 * cib * RS;   // [j][rr][ss]
-            float f[36];   // [j][r][s] of the 3 x 3 taps
-            if (R == 3 && S == 3) {
+            const int k = cib >> 1, cb = cib & 1, ci0 = CU * cib;
+            const int nj = co < co_n ? (Cin - ci0 < CU ? Cin - ci0 : CU) : 0;   // real channels of this unit
+            const float *src = raw + (size_t)co * g.raw_pitch * 4 + (size_t)ci0 * RS;   // [j][rr][ss]
+            float f[CU * 9];   // [j][r][s] of the 3 x 3 taps
+            if (R == 3 && S == 3 && nj == CU) {
 #pragma unroll
-                for (int q = 0; q < 9; ++q) {
-                    const float4 v = ok ? *reinterpret_cast<const float4 *>(src + 4 * q) : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int q = 0; q < CU * 9 / 4; ++q) {
+                    const float4 v = *reinterpret_cast<const float4 *>(src + 4 * q);
                     f[4 * q] = v.x;
                     f[4 * q + 1] = v.y;
                     f[4 * q + 2] = v.z;
@@ -298,24 +352,32 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
                 }
             } else {
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
+                for (int j = 0; j < CU; ++j)
 #pragma unroll
                     for (int t = 0; t < 9; ++t) {
                         const int rr = t / 3 - (3 - R) / 2, ss = t % 3 - (3 - S) / 2;
-                        f[j * 9 + t] = (ok && rr >= 0 && rr < R && ss >= 0 && ss < S) ? src[j * RS + rr * S + ss] : 0.f;
+                        f[j * 9 + t] = (j < nj && rr >= 0 && rr < R && ss >= 0 && ss < S) ? src[j * RS + rr * S + ss] : 0.f;
                     }
             }
 #pragma unroll
             for (int t = 0; t < 9; ++t) {
                 const int r = t / 3, s = t % 3;
-                bank[((k * 3 + r) * 2 + cb) * NB + s * CG + co] = make_float4(f[t], f[9 + t], f[18 + t], f[27 + t]);
+                uint4 o;
+                if constexpr (CU == 4) {
+                    o = make_uint4(__float_as_uint(f[t]), __float_as_uint(f[9 + t]), __float_as_uint(f[18 + t]),
+                                   __float_as_uint(f[27 + t]));
+                } else {
+                    o = make_uint4(tc::pack_bf16(f[t], f[9 + t]), tc::pack_bf16(f[18 + t], f[27 + t]),
+                                   tc::pack_bf16(f[36 + t], f[45 + t]), tc::pack_bf16(f[54 + t], f[63 + t]));
+                }
+                bank[((k * 3 + r) * 2 + cb) * NB + s * CG + co] = o;
             }
         }
         // B rows n >= 3 * CG (N rounded up to a multiple of 16) are zero
         constexpr int PADN = NB - 3 * CG;
         if constexpr (PADN > 0) {
             for (int e = lt; e < g.nk * 3 * 2 * PADN; e += LT)
-                bank[(e / PADN) * NB + 3 * CG + e % PADN] = make_float4(0.f, 0.f, 0.f, 0.f);
+                bank[(e / PADN) * NB + 3 * CG + e % PADN] = make_uint4(0u, 0u, 0u, 0u);
         }
         // the staged weights' buffers go to the TMA (async proxy) next, the
         // bank to the tensor core
@@ -354,8 +416,10 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
                     break;
                 }
                 mbar_arrive_expect_tx(smem_u32(&full_bar[s]), g.stage_bytes);
-                tma_load_4d(smem_u32(abuf + (size_t)s * g.stage_bytes), &tmx, tc::CH * c, x0 - 1, y0 - 1, n,
-                            smem_u32(&full_bar[s]));
+#pragma unroll
+                for (int sb = 0; sb < OP::SUB; ++sb)
+                    tma_load_4d(smem_u32(abuf + (size_t)s * g.stage_bytes + (size_t)sb * (g.stage_bytes / OP::SUB)), &tmx,
+                                tc::CH * c + sb * (tc::CH / OP::SUB), x0 - 1, y0 - 1, n, smem_u32(&full_bar[s]));
                 issued = j + 1;
                 if (++s == ns) {
                     s = 0;
@@ -373,26 +437,30 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
     } else if (warp == 5) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = tc::idesc_tf32(NB);
+            constexpr uint32_t idesc = tc::idesc_mma(OP::FMT, NB);
+            constexpr uint32_t A_HI = tc::a_hi<OP>();
+            constexpr uint32_t AR = 2 * OP::ROWB, AM = 8 * OP::ROWB;   // A units per vertical tap (32 rows), per M-tile (128 rows)
+            const uint32_t asub = (g.stage_bytes / OP::SUB) >> 4;         // A units per sub-buffer
             const uint32_t a_base = smem_u32(abuf) >> 4, w_base = smem_u32(wsm) >> 4;
             const uint32_t a_lbo = 1u << 16, b_lbo = (uint32_t)NB << 16;
             // G M-tiles at a time, M-tiles innermost: consecutive MMAs go to
             // different accumulators (back-to-back MMAs into one accumulator
-            // issue more slowly); a full stage (4 K steps) is unrolled so that
-            // every descriptor is a register plus a constant.  A: +2 units (32 B) per K step, +256 units
-            // (4 KB) per vertical tap, +1024 units (16 KB) per M-tile.  B:
+            // issue more slowly); a full stage (KS K steps) is unrolled so that
+            // every descriptor is a register plus a constant.  A: +2 units
+            // (32 B) per K step within a row, asub per sub-buffer, AR per
+            // vertical tap, AM per M-tile.  B:
             // 2 * NB units per (K step, tap).
             auto issue = [&](auto gsz, uint32_t d0, uint32_t a0, uint32_t b0, int nks, uint32_t acc0) {
                 constexpr int G = decltype(gsz)::value;
-                if (nks == 4) {
+                if (nks == KS) {
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
+                    for (int kk = 0; kk < KS; ++kk)
 #pragma unroll
                         for (int r = 0; r < 3; ++r)
 #pragma unroll
                             for (int gi = 0; gi < G; ++gi)
-                                tc::mma_tf32_w(d0 + (uint32_t)(gi * NB), a0 + (uint32_t)(kk * 2 + r * 256 + gi * 1024),
-                                               tc::A_HI, b0 + (uint32_t)((kk * 3 + r) * 2 * NB), tc::B_HI, idesc,
+                                tc::mma_w<OP>(d0 + (uint32_t)(gi * NB), a0 + (uint32_t)(kk / KSUB) * asub + (uint32_t)((kk % KSUB) * 2 + r * AR + gi * AM),
+                                               A_HI, b0 + (uint32_t)((kk * 3 + r) * 2 * NB), tc::B_HI, idesc,
                                                (kk > 0 || r > 0) ? 1u : acc0);
                     return;
                 }
@@ -402,8 +470,8 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
                     for (int r = 0; r < 3; ++r)
 #pragma unroll
                         for (int gi = 0; gi < G; ++gi)
-                            tc::mma_tf32_w(d0 + (uint32_t)(gi * NB), a0 + (uint32_t)(kk * 2 + r * 256 + gi * 1024),
-                                           tc::A_HI, b0 + (uint32_t)((kk * 3 + r) * 2 * NB), tc::B_HI, idesc,
+                            tc::mma_w<OP>(d0 + (uint32_t)(gi * NB), a0 + (uint32_t)(kk / KSUB) * asub + (uint32_t)((kk % KSUB) * 2 + r * AR + gi * AM),
+                                           A_HI, b0 + (uint32_t)((kk * 3 + r) * 2 * NB), tc::B_HI, idesc,
                                            (kk > 0 || r > 0) ? 1u : acc0);
                 }
             };
@@ -426,8 +494,8 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
                     }
                     tc::fence_after_sync();
                     const uint32_t a_lo = (a_base + (uint32_t)s * (g.stage_bytes >> 4)) | a_lbo;
-                    const uint32_t b_lo = (w_base + (uint32_t)(c * 4 * 3 * 2 * NB)) | b_lbo;
-                    const int nks = g.nk - 4 * c < 4 ? g.nk - 4 * c : 4;
+                    const uint32_t b_lo = (w_base + (uint32_t)(c * KS * 3 * 2 * NB)) | b_lbo;
+                    const int nks = g.nk - KS * c < KS ? g.nk - KS * c : KS;
                     const uint32_t acc0 = c > 0 ? 1u : 0u;
                     int mt = 0;
                     if (g.MT == 1) {
@@ -439,7 +507,7 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
                     }
 #pragma unroll 1
                     for (; mt < g.MT; mt += 2)
-                        issue(std::integral_constant<int, 2>{}, dbase + (uint32_t)(mt * NB), a_lo + (uint32_t)(mt * 1024),
+                        issue(std::integral_constant<int, 2>{}, dbase + (uint32_t)(mt * NB), a_lo + (uint32_t)(mt * AM),
                               b_lo, nks, acc0);
                     tc::mma_commit(smem_u32(&empty_bar[s]));
                     committed = j;
@@ -458,23 +526,24 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
             if (committed >= 0)
                 (void)mbar_wait_bounded(smem_u32(&empty_bar[committed % ns]), (committed / ns) & 1, timeout_ns);
         }
-    } else if (warp < 4) {
+    } else {
         // ------------------------------------------------------------ epilogue
-        // Lane l of warp w holds GEMM row m = mt * 128 + 32 w + l, i.e. padded
-        // column l of tile row 4 mt + w; its output column l (l < 30) is the
+        // Two sets of four warps (0-3 and 6-9); warp w reads TMEM lane
+        // quadrant q = w % 4, set 0 the even M-tiles of a tile, set 1 the odd
+        // ones.  Lane l holds GEMM row m = mt * 128 + 32 q + l, i.e. padded
+        // column l of tile row 4 mt + q; its output column l (l < 30) is the
         // sum over s of the s-block of lane l + s.  With TMA_OUT each lane
         // writes its pixel (bias and ReLU applied) into the warp's output
         // buffer and lane 0 stores the row with one TMA copy (image edges and
-        // channels past Cout are clipped by the TMA); the warp's two buffers
-        // alternate, lane 0 waiting for the store that last read one before
-        // it is refilled.  Otherwise (CW of 4 or 8 channels, 16 or 32 bytes
-        // per pixel) each lane stores its pixel directly: neighbouring lanes
-        // write neighbouring pixels.
+        // channels past Cout are clipped by the TMA), waiting first for its
+        // previous store to have read the buffer.  Otherwise (outputs of 16
+        // or 32 bytes per pixel) each lane stores its pixel directly:
+        // neighbouring lanes write neighbouring pixels.
+        const int q4 = warp & 3, set = warp < 4 ? 0 : 1;
         float bias_r[CW];
 #pragma unroll
         for (int i = 0; i < CW; ++i) bias_r[i] = (bias && co0 + i < Cout) ? __ldg(bias + co0 + i) : 0.f;
-        const uint32_t wst = smem_u32(stg + warp * 2 * tc::OUT_BUF);
-        int nstore = 0;
+        const uint32_t wst = smem_u32(stg + (warp < 4 ? warp : warp - 2) * tc::OUT_BUF);
         for (int u = 0; u < my_tiles; ++u) {
             const int b = u & 1;
             if (aborted()) break;
@@ -486,15 +555,22 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
             tc::fence_after_sync();
             int n, y0, x0;
             tile_origin(u, n, y0, x0);
-            const uint32_t tbuf = tmem + (uint32_t)(b * tc::TMEM_BUF) + ((uint32_t)(warp * 32) << 16);
-            for (int mt = 0; mt < g.MT; ++mt) {
+            const uint32_t tbuf = tmem + (uint32_t)(b * tc::TMEM_BUF) + ((uint32_t)(q4 * 32) << 16);
+            const int last_mt = set + ((g.MT - 1 - set) & ~1);   // this set's last M-tile (< set: none)
+            if (last_mt < set) {
+                // nothing of this tile for this warp: release the buffer at once
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&acc_empty[b]));
+            }
+            for (int mt = set; mt < g.MT; mt += 2) {
                 uint32_t r0[CW], r1[CW], r2[CW];
                 tc::tmem_ld<CW>(tbuf + (uint32_t)(mt * NB), r0);
                 tc::tmem_ld<CW>(tbuf + (uint32_t)(mt * NB + CG), r1);
                 tc::tmem_ld<CW>(tbuf + (uint32_t)(mt * NB + 2 * CG), r2);
                 tc::tmem_wait_ld();
-                if (mt == g.MT - 1) {
-                    // every column of this buffer is in registers: release it
+                if (mt == last_mt) {
+                    // every column this warp needs is in registers: release the buffer
                     tc::fence_before_sync();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&acc_empty[b]));
@@ -505,17 +581,22 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
                     v[i] = relu_if(__uint_as_float(r0[i]) + __shfl_down_sync(0xffffffffu, __uint_as_float(r1[i]), 1) +
                                        __shfl_down_sync(0xffffffffu, __uint_as_float(r2[i]), 2) + bias_r[i],
                                    act);
-                const int oy = y0 + mt * 4 + warp;
+                // the pixel's outputs as 32-bit words: fp32, or bf16 pairs
+                constexpr int NWD = CW * OSZ / 4;
+                uint32_t o[NWD];
+#pragma unroll
+                for (int i = 0; i < NWD; ++i) o[i] = YBF16 ? tc::pack_bf16(v[2 * i], v[2 * i + 1]) : __float_as_uint(v[i]);
+                const int oy = y0 + mt * 4 + q4;
                 if (oy >= H) continue;   // the same for the whole warp
                 if constexpr (TMA_OUT) {
-                    const uint32_t ob = wst + (uint32_t)((nstore & 1) * tc::OUT_BUF);
-                    if (lane == 0) bulk_wait_read<1>();   // the store that last read this buffer is done
+                    const uint32_t ob = wst;
+                    if (lane == 0) bulk_wait_read<0>();   // the store that last read this buffer is done
                     __syncwarp();
                     if (lane < tc::TC) {
 #pragma unroll
-                        for (int q = 0; q < CPR; ++q)
-                            tc::st_shared_v4(ob + lane * (CW * 4) + ((q ^ tc::stg_key<CW>(lane)) << 4), v[4 * q],
-                                             v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                        for (int q = 0; q < OCH; ++q)
+                            tc::st_shared_v4(ob + lane * OROWB + ((q ^ tc::stg_key<OROWB>(lane)) << 4), o[4 * q],
+                                             o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
                     }
                     fence_proxy_async_smem();   // these writes -> visible to the TMA
                     __syncwarp();
@@ -523,16 +604,22 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
                         tma_store_4d(&tmy, ob, co0, x0, oy, n);
                         bulk_commit();
                     }
-                    ++nstore;
                 } else {
+                    // pieces of 4 channels: 16 bytes (fp32) or 8 bytes (bf16)
                     const int ox = x0 + lane;
                     if (lane < tc::TC && ox < W) {
-                        float *yp = y + (((long long)n * H + oy) * W + ox) * Cout + co0;
+                        unsigned char *yp = reinterpret_cast<unsigned char *>(yv) +
+                                            ((((long long)n * H + oy) * W + ox) * Cout + co0) * OSZ;
 #pragma unroll
-                        for (int q = 0; q < CPR; ++q)
-                            if (co0 + 4 * q < Cout)
-                                *reinterpret_cast<float4 *>(yp + 4 * q) =
-                                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                        for (int q = 0; q < CW / 4; ++q) {
+                            if (co0 + 4 * q < Cout) {
+                                if constexpr (YBF16)
+                                    *reinterpret_cast<uint2 *>(yp + 8 * q) = make_uint2(o[2 * q], o[2 * q + 1]);
+                                else
+                                    *reinterpret_cast<uint4 *>(yp + 16 * q) =
+                                        make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                            }
+                        }
                     }
                 }
             }
@@ -558,9 +645,10 @@ constexpr size_t kTcSmemCap = 227 * 1024 - 1024;
 // those, the MT that wastes least work on halo rows, partial tiles and an
 // unevenly filled persistent grid.  Leftover shared memory goes to further
 // stage buffers (up to MAX_STAGE).
-static bool tc_geometry(int Cg, int NB, int groups, int Cin, int RS, int H, int W, int Nimg, tc::TcGeom &g)
+static bool tc_geometry(int Cg, int NB, int kc, int rowb, int groups, int Cin, int RS, int H, int W, int Nimg,
+                        tc::TcGeom &g)
 {
-    const int nk = (Cin + 7) / 8;
+    const int nk = (Cin + kc - 1) / kc;
     const size_t w_bytes = ((size_t)nk * 3 * 2 * NB * 16 + 1023) & ~(size_t)1023;
     const size_t fixed = w_bytes + tc::STG_BYTES + 1024;   // + alignment slack
     if (fixed >= kTcSmemCap) return false;
@@ -574,7 +662,7 @@ static bool tc_geometry(int Cg, int NB, int groups, int Cin, int RS, int H, int 
     const size_t raw = (size_t)Cg * raw_pitch * 16;
     for (int MT = 1; MT * NB <= tc::TMEM_BUF && MT <= 16; ++MT) {
         const int TR = 4 * MT;
-        const size_t stage = (size_t)(TR + 2) * tc::WP * tc::CH * 4;
+        const size_t stage = (size_t)(TR + 2) * tc::WP * rowb;
         if (fixed + tc::MIN_STAGE * stage > kTcSmemCap) break;
         const size_t nfit = (kTcSmemCap - fixed) / stage;
         if ((nfit < tc::MAX_STAGE ? nfit : tc::MAX_STAGE) * stage < raw) continue;
@@ -598,7 +686,7 @@ static bool tc_geometry(int Cg, int NB, int groups, int Cin, int RS, int H, int 
     g.ntiles = g.tiles_x * g.tiles_y * Nimg;
     g.nk = nk;
     g.nstg = (Cin + tc::CH - 1) / tc::CH;
-    g.stage_bytes = (uint32_t)((size_t)g.THh * tc::WP * tc::CH * 4);
+    g.stage_bytes = (uint32_t)((size_t)g.THh * tc::WP * rowb);
     g.w_bytes = (uint32_t)w_bytes;
     const int ns = (int)((kTcSmemCap - fixed) / g.stage_bytes);
     g.nstage = ns < tc::MAX_STAGE ? ns : tc::MAX_STAGE;
@@ -623,41 +711,49 @@ static PFN_cuTensorMapEncodeTiled_v12000 tc_tensor_map_encoder()
     return fn;
 }
 
-template <int CG>
+// a.x and a.y point to fp32 or (for OP = OpBF16, YBF16) bf16 NHWC tensors.
+template <int CG, class OP, bool YBF16>
 static cudaError_t launch_tc_cg(const ConvArgs &a, cudaStream_t st)
 {
     constexpr int NB = (3 * CG + 15) / 16 * 16;
+    constexpr int OSZ = YBF16 ? 2 : 4;
+    constexpr int OROWB = CG * OSZ;
     tc::TcGeom g;
     const int groups = (a.Cout + CG - 1) / CG;
-    if (!tc_geometry(CG, NB, groups, a.Cin, a.R * a.S, a.H, a.W, a.N, g)) return cudaErrorNotSupported;
+    if (!tc_geometry(CG, NB, OP::KC, OP::ROWB * OP::SUB, groups, a.Cin, a.R * a.S, a.H, a.W, a.N, g))
+        return cudaErrorNotSupported;
     if ((long long)g.tiles_x * g.tiles_y * a.N > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     PFN_cuTensorMapEncodeTiled_v12000 encode = tc_tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
-    // NHWC activations as a 4-D tensor (C, W, H, N); box = 32 channels (one
-    // 128-byte swizzled row per pixel; channels past Cin read as zero) x 32
-    // padded columns x (TR + 2) rows of one image
+    // NHWC activations as a 4-D tensor (C, W, H, N); box = the channels of
+    // one sub-buffer (32 fp32 or 16 bf16: one swizzled row per pixel;
+    // channels past Cin read as zero) x 32 padded columns x (TR + 2) rows of
+    // one image
     CUtensorMap tm;
     const cuuint64_t dims[4] = {(cuuint64_t)a.Cin, (cuuint64_t)a.W, (cuuint64_t)a.H, (cuuint64_t)a.N};
-    const cuuint64_t strides[3] = {(cuuint64_t)a.Cin * 4, (cuuint64_t)a.W * a.Cin * 4,
-                                   (cuuint64_t)a.H * a.W * a.Cin * 4};
-    const cuuint32_t box[4] = {(cuuint32_t)tc::CH, (cuuint32_t)tc::WP, (cuuint32_t)g.THh, 1};
+    const cuuint64_t strides[3] = {(cuuint64_t)a.Cin * OP::ESZ, (cuuint64_t)a.W * a.Cin * OP::ESZ,
+                                   (cuuint64_t)a.H * a.W * a.Cin * OP::ESZ};
+    const cuuint32_t box[4] = {(cuuint32_t)(tc::CH / OP::SUB), (cuuint32_t)tc::WP, (cuuint32_t)g.THh, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
-    if (encode(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(a.x), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    if (encode(&tm, OP::ESZ == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+               const_cast<float *>(a.x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               OP::ROWB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_32B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorNotSupported;
     // NHWC output as (C, W, H, N); box = the group's CG channels x TC pixels
-    // of one row, swizzled like the epilogue's buffers (groups of 16 or 32
-    // channels; smaller groups store directly and leave this map unused)
+    // of one row, swizzled like the epilogue's buffers (groups whose outputs
+    // take 64 or 128 bytes per pixel; the others store directly and leave
+    // this map unused)
     CUtensorMap tmo;
     std::memset(&tmo, 0, sizeof(tmo));
-    if (CG >= 16) {
+    if (OROWB >= 64) {
         const cuuint64_t odims[4] = {(cuuint64_t)a.Cout, (cuuint64_t)a.W, (cuuint64_t)a.H, (cuuint64_t)a.N};
-        const cuuint64_t ostrides[3] = {(cuuint64_t)a.Cout * 4, (cuuint64_t)a.W * a.Cout * 4,
-                                        (cuuint64_t)a.H * a.W * a.Cout * 4};
+        const cuuint64_t ostrides[3] = {(cuuint64_t)a.Cout * OSZ, (cuuint64_t)a.W * a.Cout * OSZ,
+                                        (cuuint64_t)a.H * a.W * a.Cout * OSZ};
         const cuuint32_t obox[4] = {(cuuint32_t)CG, (cuuint32_t)tc::TC, 1, 1};
-        if (encode(&tmo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.y, odims, ostrides, obox, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CG == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+        if (encode(&tmo, YBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.y, odims,
+                   ostrides, obox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   OROWB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorNotSupported;
     }
@@ -667,30 +763,39 @@ static cudaError_t launch_tc_cg(const ConvArgs &a, cudaStream_t st)
     static int allowed[64] = {0};
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (allowed[dev] < (int)g.smem_bytes) {
-        e = cudaFuncSetAttribute(conv_tc_kernel<CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem_bytes);
+        e = cudaFuncSetAttribute(conv_tc_kernel<CG, OP, YBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)g.smem_bytes);
         if (e != cudaSuccess) return e;
         allowed[dev] = (int)g.smem_bytes;
     }
     const int per_group = device_sm_count() / groups > 0 ? device_sm_count() / groups : 1;
     const int grid = g.ntiles < per_group ? g.ntiles : per_group;
-    conv_tc_kernel<CG><<<dim3(grid, groups), tc::NTHREADS, g.smem_bytes, st>>>(
+    conv_tc_kernel<CG, OP, YBF16><<<dim3(grid, groups), tc::NTHREADS, g.smem_bytes, st>>>(
         tm, tmo, a.w, a.b, a.y, a.H, a.W, a.Cin, a.Cout, a.R, a.S, a.act, g, device_status_ptr(), 1000000000ull);
     return cudaGetLastError();
 }
 
-cudaError_t launch_conv_tc(const ConvArgs &a, cudaStream_t st)
+// Output channels per CTA: the smallest group that holds Cout, at most 32
+// (larger Cout runs as groups on blockIdx.y); where a group's filters do not
+// fit in shared memory, smaller groups (a smaller MMA N, lower tensor-core
+// efficiency).
+template <class OP, bool YBF16>
+static cudaError_t launch_tc_groups(const ConvArgs &a, cudaStream_t st)
 {
     if (a.R > 3 || a.S > 3) return cudaErrorNotSupported;
-    // output channels per CTA: the smallest group that holds Cout, at most 32
-    // (larger Cout runs as groups on blockIdx.y); where a group's filters do
-    // not fit in shared memory, smaller groups (a smaller MMA N, lower
-    // tensor-core efficiency)
     cudaError_t e = cudaErrorNotSupported;
-    if (a.Cout > 16) e = launch_tc_cg<32>(a, st);
-    if (e == cudaErrorNotSupported && a.Cout > 8) e = launch_tc_cg<16>(a, st);
-    if (e == cudaErrorNotSupported && a.Cout > 4) e = launch_tc_cg<8>(a, st);
-    if (e == cudaErrorNotSupported) e = launch_tc_cg<4>(a, st);
+    if (a.Cout > 16) e = launch_tc_cg<32, OP, YBF16>(a, st);
+    if (e == cudaErrorNotSupported && a.Cout > 8) e = launch_tc_cg<16, OP, YBF16>(a, st);
+    if (e == cudaErrorNotSupported && a.Cout > 4) e = launch_tc_cg<8, OP, YBF16>(a, st);
+    if (e == cudaErrorNotSupported) e = launch_tc_cg<4, OP, YBF16>(a, st);
     return e;
+}
+
+cudaError_t launch_conv_tc(const ConvArgs &a, cudaStream_t st) { return launch_tc_groups<tc::OpTF32, false>(a, st); }
+
+cudaError_t launch_conv_tc_bf16(const ConvArgs &a, bool y_bf16, cudaStream_t st)
+{
+    return y_bf16 ? launch_tc_groups<tc::OpBF16, true>(a, st) : launch_tc_groups<tc::OpBF16, false>(a, st);
 }
 
 }  // namespace sc

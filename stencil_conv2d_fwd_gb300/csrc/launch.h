@@ -25,9 +25,12 @@ cudaError_t launch_conv_general_k7(const ConvArgs &a, cudaStream_t st);
 // kernel for K = max(R, S) (api.cu).
 cudaError_t launch_conv_nhwc(const ConvArgs &a, cudaStream_t st);
 
-// Tensor-core (tcgen05, TF32) implicit-GEMM convolution, NHWC, Cin % 4 == 0,
+// Tensor-core (tcgen05) implicit-GEMM convolution, TF32 operands, NHWC, Cin % 4 == 0,
 // Cout <= 128, R, S <= 3 (conv_tc.cu).  cudaErrorNotSupported otherwise.
 cudaError_t launch_conv_tc(const ConvArgs &a, cudaStream_t st);
+// BF16 operands (conv_tc.cu): a.x is a bf16 NHWC tensor, a.y bf16 (y_bf16)
+// or fp32; a.w, a.b fp32.
+cudaError_t launch_conv_tc_bf16(const ConvArgs &a, bool y_bf16, cudaStream_t st);
 
 // Single-input-channel convolution, Cout == 1 or Cout % 4 == 0 (conv_c1.cu).
 cudaError_t launch_conv_c1(const ConvArgs &a, cudaStream_t st);
