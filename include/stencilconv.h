@@ -181,6 +181,43 @@ int sc_version(void);
 int sc_release_workspace(void);
 
 /*
+ * sc_set_autotune: first-call autotuning of conv2d_fwd's tile configuration
+ * ("Optimizing Memory Efficiency for Convolution Kernels on Kepler GPUs",
+ * Table 1: the best configuration differs per filter size and is found by
+ * measurement).  With enable != 0, the first conv2d_fwd (NHWC or NCHW, or
+ * conv2d_fwd_nchw_noalloc) of each shape with 3 x 3 filters and Cin > 1
+ * times every candidate configuration of its output-channel class on the
+ * caller's stream and data, which synchronises that stream once; the
+ * fastest is cached per device and shape (N, H, W, Cin, Cout, R, S, act,
+ * bias present) and used by later calls.  While the stream is being captured
+ * into a CUDA graph no timing happens (the default configuration runs and
+ * nothing is cached).  Off by default.  Returns the previous setting.
+ */
+int sc_set_autotune(int enable);
+
+/* sc_autotune_lookup: the cached candidate index (0 = the default
+ * configuration) for a shape on the current device, or -1 if not tuned. */
+int sc_autotune_lookup(int N, int H, int W, int Cin, int Cout, int R, int S, int act, int has_bias);
+
+/* sc_autotune_clear: forget every cached choice. */
+void sc_autotune_clear(void);
+
+/* sc_autotune_candidates: number of candidate configurations for a filter
+ * shape (0 if not tuned); if names != NULL, their names, one per line, into
+ * names[0 .. names_len-1] (NUL-terminated, truncated to fit). */
+int sc_autotune_candidates(int Cin, int Cout, int R, int S, char *names, int names_len);
+
+/*
+ * sc_test_conv_candidate: test hook, not part of the operation.  Runs
+ * conv2d_fwd (NHWC, 3 x 3) with candidate configuration `candidate` of
+ * sc_autotune_candidates; SC_ERR_UNSUPPORTED if it does not exist or does
+ * not apply to the shape.
+ */
+int sc_test_conv_candidate(const float *x, const float *w, const float *b, float *y,
+                           int N, int H, int W, int Cin, int Cout, int R, int S,
+                           int act, int candidate, sc_stream_t stream);
+
+/*
  * sc_test_stencil_wait_expiry: test hook for the device-status path, not
  * part of the operation.  Runs stencil_pipeline_fwd's TMA kernel with the
  * copy of row chunk `drop_copy` (0-based, per warp) never issued, so each

@@ -48,6 +48,11 @@ SIGNATURES = {
     "sc_measure_ffma_peak": (_I, [_P, _I, _I, _P]),
     "sc_version": (_I, []),
     "sc_release_workspace": (_I, []),
+    "sc_set_autotune": (_I, [_I]),
+    "sc_autotune_lookup": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _I]),
+    "sc_autotune_clear": (None, []),
+    "sc_autotune_candidates": (_I, [_I, _I, _I, _I, ctypes.c_char_p, _I]),
+    "sc_test_conv_candidate": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "conv2d_fwd_nchw_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "sc_test_stencil_wait_expiry": (_I, [_P, _P, _I, _I, _I, _I, _P]),
 }
@@ -149,6 +154,33 @@ def sc_measure_ffma_peak(sink, blocks, iters, stream=None) -> int:
 
 def sc_version() -> int:
     return load().sc_version()
+
+
+def sc_set_autotune(enable) -> int:
+    """First-call autotuning of conv2d_fwd's tile configuration on/off (see the header)."""
+    return load().sc_set_autotune(1 if enable else 0)
+
+
+def sc_autotune_lookup(N, H, W, Cin, Cout, R, S, act=SC_ACT_NONE, has_bias=True) -> int:
+    return load().sc_autotune_lookup(N, H, W, Cin, Cout, R, S, act, 1 if has_bias else 0)
+
+
+def sc_autotune_clear() -> None:
+    load().sc_autotune_clear()
+
+
+def sc_autotune_candidates(Cin, Cout, R, S) -> list:
+    """Names of the candidate configurations for a filter shape ([] if not tuned)."""
+    buf = ctypes.create_string_buffer(4096)
+    n = load().sc_autotune_candidates(Cin, Cout, R, S, buf, len(buf))
+    names = buf.value.decode().split("\n")
+    return [x for x in names if x][:n]
+
+
+def sc_test_conv_candidate(x, w, b, y, N, H, W, Cin, Cout, R, S, act, candidate, stream=None) -> int:
+    """Test hook: conv2d_fwd with one candidate configuration (see the header)."""
+    return load().sc_test_conv_candidate(_ptr(x), _ptr(w), _ptr(b), _ptr(y), N, H, W, Cin, Cout, R, S, act,
+                                         candidate, _stream(stream))
 
 
 def sc_release_workspace() -> int:

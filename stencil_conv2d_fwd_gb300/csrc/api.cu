@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "../../include/stencilconv.h"
+#include "autotune.h"
 #include "launch.h"
 
 namespace {
@@ -58,6 +59,7 @@ namespace sc {
 
 cudaError_t launch_conv_nhwc(const ConvArgs &a, cudaStream_t st)
 {
+    if (autotune_enabled() && a.R == 3 && a.S == 3 && a.Cin > 1) return launch_conv_tuned(a, st);
     if (a.Cin == 1) return launch_conv_c1(a, st);
     switch (a.R > a.S ? a.R : a.S) {
     case 1: return launch_conv_general_k1(a, st);
@@ -331,6 +333,25 @@ int sc_measure_ffma_peak(float *sink, int blocks, int iters, sc_stream_t stream)
 }
 
 int sc_version(void) { return 100; }
+
+int sc_test_conv_candidate(const float *x, const float *w, const float *b, float *y, int N, int H, int W, int Cin,
+                           int Cout, int R, int S, int act, int candidate, sc_stream_t stream)
+{
+    if (!x || !w || !y) return SC_ERR_NULL;
+    if (checked_count({N, H, W, Cin}) < 0 || checked_count({N, H, W, Cout}) < 0) return SC_ERR_SHAPE;
+    if (R != 3 || S != 3 || Cin < 2 || (Cin % 4) != 0 || (Cout % 4) != 0) return SC_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(y)) return SC_ERR_ALIGN;
+    sc::ConvArgs a{x, w, b, y, N, H, W, Cin, Cout, R, S, act};
+    const sc::TuneCand *c = nullptr;
+    const int n = sc::k3_candidates(a, &c);
+    if (candidate < 0 || candidate >= n) return SC_ERR_UNSUPPORTED;
+    const cudaError_t e = c[candidate].launch(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) {
+        cudaGetLastError();
+        return SC_ERR_UNSUPPORTED;
+    }
+    return e == cudaSuccess ? SC_OK : cuda_fail(e);
+}
 
 int sc_release_workspace(void)
 {

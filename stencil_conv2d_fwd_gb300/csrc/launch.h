@@ -49,6 +49,11 @@ cudaError_t launch_transpose_batched(const float *src, float *dst, int N, long l
 // FP32 FMA rate probe (peak.cu).
 cudaError_t launch_ffma_peak(float *sink, int blocks, int iters, cudaStream_t st);
 
+// First-call autotuner (autotune.cu): whether sc_set_autotune turned it on,
+// and conv2d_fwd for NHWC tensors through it (3 x 3 filters, Cin > 1).
+bool autotune_enabled();
+cudaError_t launch_conv_tuned(const ConvArgs &a, cudaStream_t st);
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
