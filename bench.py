@@ -43,7 +43,7 @@ FP32_LANES_PER_SM = 128          # FP32 FMA lanes per Blackwell SM (4 schedulers
 ONLY_CASES = {
     "1": (1, 0), "2": (2, 0), "3-L1": (3, 0), "3-L2": (3, 1), "3-L3": (3, 2), "4": (4, 0), "5": (5, None),
     "4-tc": (4, 0), "3-L2-tc": (3, 1), "3-L3-tc": (3, 2),
-    "4-bf16": (4, 0), "3-L2-bf16": (3, 1), "3-L3-bf16": (3, 2),
+    "4-bf16": (4, 0), "3-L2-bf16": (3, 1), "3-L3-bf16": (3, 2), "3-L23-fused": (3, 1),
 }
 
 
@@ -507,6 +507,34 @@ def per_config(sc, S, dev, stream, flush, fp32_tflops, hbm_gbs, hbm_src):
                      "tolerance": "5e-3 * sum|x*w| + 2^-8 |y| (bf16 operands and storage)",
                      "bf16_peak_tflops": round(bf16_tflops, 1)}
 
+    # layer fusion (f2): layers 2 and 3 of the net in one tensor-core pass,
+    # the 32-channel intermediate kept on chip (TF32 operands)
+    wl = S.config(3)
+    L2, L3 = wl.layers[1], wl.layers[2]
+    xin = np.maximum(S.uniform(77, 0, (wl.n, L2.cin, wl.h, wl.w), -1, 1), 0)
+    xd = torch.from_numpy(np.ascontiguousarray(xin.transpose(0, 2, 3, 1)).astype(np.float32)).to(dev)
+    w2d, b2d = torch.from_numpy(L2.w).to(dev), torch.from_numpy(L2.b).to(dev)
+    w3d, b3d = torch.from_numpy(L3.w).to(dev), torch.from_numpy(L3.b).to(dev)
+    yd = torch.empty(wl.n * wl.h * wl.w * L3.cout, device=dev)
+
+    def call_fused(s=None):
+        rc = sc.conv2d_fwd_tc_fused2(xd, w2d, b2d, w3d, b3d, yd, wl.n, wl.h, wl.w, L2.cin, L2.cout, L3.cout,
+                                     L2.act, L3.act, s if s is not None else stream)
+        if rc != 0:
+            raise RuntimeError(sc.sc_status_string(rc))
+    med, mn = time_events(call_fused, stream, flush, reps=20)
+    flops = conv_flops(wl.n, wl.h, wl.w, L2) + conv_flops(wl.n, wl.h, wl.w, L3)
+    byts = 4 * (wl.n * wl.h * wl.w * (L2.cin + L3.cout) + L2.w.size + L2.b.size + L3.w.size + L3.b.size)
+    t_c, t_m = flops / (tf32_tflops * 1e12), byts / (hbm_gbs * 1e9)
+    out["3-L2+3-L3 fused (tcgen05 TF32)"] = {
+        "ms_median": round(med, 5), "ms_min": round(mn, 5),
+        "gflops": round(flops / (med * 1e-3) / 1e9, 2),
+        "mpixel_per_s": round(wl.n * wl.h * wl.w / (med * 1e-3) / 1e6, 2),
+        "roofline_bound": "tensor" if t_c >= t_m else "hbm",
+        "roofline_us": round(max(t_c, t_m) * 1e6, 3),
+        "roofline_frac": round(max(t_c, t_m) / (med * 1e-3), 4),
+        "note": "FLOP and bytes are the two layers' algorithmic counts; the intermediate never reaches HBM"}
+
     c5 = S.config(5)
     ind = torch.from_numpy(c5.img).to(dev)
     outd = torch.empty_like(ind)
@@ -643,6 +671,12 @@ def run_only(args, local):
                 x = y
         if args.only.endswith("-tc"):   # the tensor-core (TF32) variant
             launch = lambda: sc.conv2d_fwd_tc(x, wd, bd, y, N, H, W, L.cin, L.cout, L.r, L.s, L.act)
+        elif args.only == "3-L23-fused":   # layers 2 and 3 fused on the tensor cores
+            L3 = wl.layers[2]
+            w3d, b3d = torch.from_numpy(L3.w).to(dev), torch.from_numpy(L3.b).to(dev)
+            y3 = torch.empty(N * H * W * L3.cout, device=dev)
+            launch = lambda: sc.conv2d_fwd_tc_fused2(x, wd, bd, w3d, b3d, y3, N, H, W, L.cin, L.cout, L3.cout,
+                                                     L.act, L3.act)
         elif args.only.endswith("-bf16"):   # bf16 storage, BF16 tensor-core operands
             xb = x.to(torch.bfloat16)
             yb = torch.empty(N * H * W * L.cout, dtype=torch.bfloat16, device=dev)

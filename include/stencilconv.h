@@ -117,6 +117,29 @@ int conv2d_fwd_tc_bf16(const void *x, const float *w, const float *b, void *y,
                        int act, int y_dtype, sc_stream_t stream);
 
 /*
+ * conv2d_fwd_tc_fused2: two 3 x 3 convolution layers in one pass on the
+ * tensor cores, the intermediate activation kept on chip ("Optimizing
+ * convolution kernels - CNNs in Vulkan Part 2/3", "Reducing memory traffic";
+ * "Model-Based Warp Overlapped Tiling for Image Processing Programs on GPUs",
+ * Abstract: overlapped tiles recompute the producer's halo):
+ *   t = act1(conv(x, w1) + b1),  y = act2(conv(t, w2) + b2),
+ * both "same"-padded with zeros (t is zero outside the image), TF32 operands,
+ * fp32 accumulation.  Tolerance: layer 2 of the exact t within
+ * 5e-3 * sum|t * w2|, plus layer 1's error (5e-3 * sum|x * w1| per element of
+ * t) carried through |w2|.
+ * x : N*H*W*C0 NHWC fp32.  w1 : C1*C0*3*3 OIHW.  b1 : C1 floats or NULL.
+ * w2 : C2*C1*3*3 OIHW.  b2 : C2 floats or NULL.  y : N*H*W*C2 NHWC fp32.
+ * x, y, w1, w2 16-byte aligned.
+ * Supported: C0 % 4 == 0 with C0 <= 32 or so (its filters resident in
+ *   shared memory beside two input stages), C1 == 32, C2 in {4, 8}.
+ * Returns SC_OK or a negative sc_status.
+ */
+int conv2d_fwd_tc_fused2(const float *x, const float *w1, const float *b1,
+                         const float *w2, const float *b2, float *y,
+                         int N, int H, int W, int C0, int C1, int C2,
+                         int act1, int act2, sc_stream_t stream);
+
+/*
  * stencil_pipeline_fwd: three stencil stages fused in one pass over a
  * single-channel image ("Model-Based Warp Overlapped Tiling for Image
  * Processing Programs on GPUs", Abstract: stages fused into overlapped

@@ -40,6 +40,7 @@ SIGNATURES = {
     "conv2d_fwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "conv2d_fwd_tc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "conv2d_fwd_tc_bf16": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
+    "conv2d_fwd_tc_fused2": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "stencil_pipeline_fwd": (_I, [_P, _P, _I, _I, _P]),
     "sc_repack": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "sc_last_device_status": (_I, [_P]),
@@ -123,6 +124,13 @@ def conv2d_fwd_tc_bf16(x, w, b, y, N, H, W, Cin, Cout, R, S, act=SC_ACT_NONE, y_
     """BF16-storage tensor-core variant: x bf16, y bf16 or fp32 (see the header)."""
     return load().conv2d_fwd_tc_bf16(_ptr(x), _ptr(w), _ptr(b), _ptr(y), N, H, W, Cin, Cout, R, S, act, y_dtype,
                                      _stream(stream))
+
+
+def conv2d_fwd_tc_fused2(x, w1, b1, w2, b2, y, N, H, W, C0, C1, C2, act1=SC_ACT_RELU, act2=SC_ACT_NONE,
+                         stream=None) -> int:
+    """Two 3x3 layers fused on the tensor cores, intermediate on chip (see the header)."""
+    return load().conv2d_fwd_tc_fused2(_ptr(x), _ptr(w1), _ptr(b1), _ptr(w2), _ptr(b2), _ptr(y), N, H, W, C0, C1, C2,
+                                       act1, act2, _stream(stream))
 
 
 def stencil_pipeline_fwd(inp, out, H, W, stream=None) -> int:

@@ -261,6 +261,31 @@ int conv2d_fwd_tc_bf16(const void *x, const float *w, const float *b, void *y, i
     return e == cudaSuccess ? SC_OK : cuda_fail(e);
 }
 
+int conv2d_fwd_tc_fused2(const float *x, const float *w1, const float *b1, const float *w2, const float *b2,
+                         float *y, int N, int H, int W, int C0, int C1, int C2, int act1, int act2, sc_stream_t stream)
+{
+    if (!x || !w1 || !w2 || !y) return SC_ERR_NULL;
+    const long long nx = checked_count({N, H, W, C0});
+    const long long ny = checked_count({N, H, W, C2});
+    if (nx < 0 || ny < 0 || C1 < 1) return SC_ERR_SHAPE;
+    if (H > (1 << 30) || W > (1 << 30)) return SC_ERR_SHAPE;
+    if ((act1 != SC_ACT_NONE && act1 != SC_ACT_RELU) || (act2 != SC_ACT_NONE && act2 != SC_ACT_RELU))
+        return SC_ERR_UNSUPPORTED;
+    if ((C0 % 4) != 0 || C1 != 32 || (C2 % 4) != 0 || C2 > 8) return SC_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(y) || !aligned16(w1) || !aligned16(w2)) return SC_ERR_ALIGN;
+    const size_t ybytes = (size_t)ny * sizeof(float);
+    if (overlaps(y, ybytes, x, (size_t)nx * sizeof(float)) ||
+        overlaps(y, ybytes, w1, (size_t)C1 * C0 * 9 * sizeof(float)) ||
+        overlaps(y, ybytes, w2, (size_t)C2 * C1 * 9 * sizeof(float)) ||
+        overlaps(y, ybytes, b1, b1 ? (size_t)C1 * sizeof(float) : 0) ||
+        overlaps(y, ybytes, b2, b2 ? (size_t)C2 * sizeof(float) : 0))
+        return SC_ERR_ALIAS;
+    sc::FusedArgs a{x, w1, b1, w2, b2, y, N, H, W, C0, C1, C2, act1, act2};
+    const cudaError_t e = sc::launch_conv_tc_fused2(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return SC_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? SC_OK : cuda_fail(e);
+}
+
 int stencil_pipeline_fwd(const float *in, float *out, int H, int W, sc_stream_t stream)
 {
     if (!in || !out) return SC_ERR_NULL;

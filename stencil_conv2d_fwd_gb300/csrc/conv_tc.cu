@@ -64,7 +64,6 @@
 // memory and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
-#include <cuda_bf16.h>
 
 #include <cstring>
 #include <mutex>
@@ -72,170 +71,16 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "tc_common.cuh"
 
 namespace sc {
 
 namespace tc {
-
-constexpr int NTHREADS = 320;   // warps 4 producer, 5 MMA; 0-3 and 6-9 epilogue (two sets, TMEM lane quadrant = warp % 4)
-constexpr int WP = 32;          // padded row pitch (pixels) = lanes of a warp
-constexpr int TC = 30;          // output columns per tile
-constexpr int CH = 32;          // channels per stage (one swizzled row per pixel)
 constexpr int MIN_STAGE = 2;
 constexpr int MAX_STAGE = 6;
 constexpr int TMEM_BUF = 256;   // tensor-memory columns per accumulator buffer (two buffers)
 constexpr int OUT_BUF = 4096;                // one epilogue output buffer: 30 pixel rows of up to 128 bytes
 constexpr int STG_BYTES = 8 * OUT_BUF;       // one per epilogue warp
-
-// Operand kinds.  Either way a K step (one MMA's K) is 32 bytes of a pixel's
-// channels and one 16-byte chunk of a B row holds CU = KC / 2 channels.  A
-// 32-channel stage is SUB sub-buffers, each filled by one TMA box, with one
-// ROWB-byte swizzled row per padded pixel.  The row widths are chosen so that
-// the tensor core's read of a 32-byte K slice of 8 consecutive rows touches
-// every 16-byte bank group exactly twice (no conflicts): 128-byte rows with
-// 128-byte swizzling, or 32-byte rows with 32-byte swizzling (64-byte rows
-// with 64-byte swizzling would put rows r and r + 2 on the same banks).
-//  * OpTF32: fp32 activations, TF32 MMA (kind::tf32), K step = 8 channels;
-//    one 128-byte row of 32 channels per pixel (4 K steps per row).
-//  * OpBF16: bf16 activations, BF16 MMA (kind::f16), K step = 16 channels;
-//    two sub-buffers of 32-byte rows (16 channels, one K step each).  The
-//    fp32 filters are rounded to bf16 (to nearest even) when the CTA stages
-//    them.
-struct OpTF32 {
-    static constexpr int ESZ = 4, KC = 8, ROWB = 128, SUB = 1;
-    static constexpr uint32_t A_LAYOUT = 2, FMT = 2;   // descriptor layout 128B swizzle; TF32
-};
-struct OpBF16 {
-    static constexpr int ESZ = 2, KC = 16, ROWB = 32, SUB = 2;
-    static constexpr uint32_t A_LAYOUT = 6, FMT = 1;   // descriptor layout 32B swizzle; BF16
-};
-
-// Instruction descriptor: D = F32, A = B = FMT (TF32 2, BF16 1), both
-// K-major, dense, M = 128.
-__host__ __device__ constexpr uint32_t idesc_mma(uint32_t fmt, int n)
-{
-    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(n >> 3) << 17) | ((128u >> 4) << 24);
-}
-
-// Shared-memory matrix descriptors as two 32-bit words: low = start address
-// (16-byte units, bits 0-13) | LBO (16-byte units) << 16; high = SBO
-// (16-byte units) | version 1 << 14 | layout type << 29 (bits 61-63 of the
-// descriptor; 0 = no swizzle, 2 = 128-byte swizzle); base offset 0.  Shared
-// addresses stay below 2^18, so stepping a start address is one 32-bit add
-// that cannot carry into the LBO field.
-template <class OP>
-__host__ __device__ constexpr uint32_t a_hi() { return ((8u * OP::ROWB) >> 4) | (1u << 14) | (OP::A_LAYOUT << 29); }   // SBO = 8 rows
-constexpr uint32_t B_HI = (128u >> 4) | (1u << 14);
-
-template <class OP>
-__device__ __forceinline__ void mma_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo, uint32_t b_hi,
-                                      uint32_t idesc, uint32_t acc)
-{
-    if constexpr (OP::FMT == 2) {
-        asm volatile(
-            "{\n"
-            ".reg .pred p;\n"
-            ".reg .b64 da, db;\n"
-            "setp.ne.b32 p, %6, 0;\n"
-            "mov.b64 da, {%1, %2};\n"
-            "mov.b64 db, {%3, %4};\n"
-            "tcgen05.mma.cta_group::1.kind::tf32 [%0], da, db, %5, p;\n"
-            "}\n" ::"r"(d_tmem),
-            "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc)
-            : "memory");
-    } else {
-        asm volatile(
-            "{\n"
-            ".reg .pred p;\n"
-            ".reg .b64 da, db;\n"
-            "setp.ne.b32 p, %6, 0;\n"
-            "mov.b64 da, {%1, %2};\n"
-            "mov.b64 db, {%3, %4};\n"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n"
-            "}\n" ::"r"(d_tmem),
-            "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc)
-            : "memory");
-    }
-}
-
-// Two floats -> two bf16 (round to nearest even), `lo` at the lower address.
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
-{
-    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t *>(&h);
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
-{
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(dst_smem), "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
-{
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-__device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
-__device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
-
-// CW consecutive fp32 TMEM columns (4, 8, 16 or 32) of this thread's lane;
-// the caller waits with tmem_wait_ld before using them.
-template <int CW>
-__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[CW])
-{
-    if constexpr (CW == 4) {
-        asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];\n"
-                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                     : "r"(taddr));
-    } else if constexpr (CW == 8) {
-        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
-                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-                     : "r"(taddr));
-    } else if constexpr (CW == 16) {
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
-            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-            : "r"(taddr));
-    } else {
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-            "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
-            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-              "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
-              "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
-              "=r"(r[30]), "=r"(r[31])
-            : "r"(taddr));
-    }
-}
-
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
-{
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-
-// Swizzle key of pixel row p of an epilogue output buffer (rows of ROWB =
-// 128 or 64 bytes, 1024-byte aligned): 16-byte chunk q of row p is stored at
-// chunk q ^ key(p).  This is the TMA's own 128-byte or 64-byte swizzle
-// pattern, so the buffer is a valid source for a swizzled TMA store, and the
-// row-wise writes (one row per lane) of every 8-lane phase touch 8 distinct
-// 16-byte bank groups.
-template <int ROWB>
-__device__ __forceinline__ int stg_key(int p)
-{
-    return ROWB == 128 ? (p & 7) : ((p >> 1) & 3);
-}
 
 struct TcGeom {
     int MT, TR, THh;                // M-tiles per tile, tile rows (4 * MT), staged rows (TR + 2)
@@ -330,55 +175,10 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
     } else {
         const bool landed = mbar_wait_bounded(smem_u32(&w_bar), 0, timeout_ns);
         if (!landed) give_up_flag(abort_sh);
-        const float *raw = reinterpret_cast<const float *>(raw_sm);
-        uint4 *bank = reinterpret_cast<uint4 *>(wsm);
         constexpr int LT = tc::NTHREADS - 32;   // threads of every warp but the producer
-        const int lt = warp < 4 ? tid : tid - 32;
-        const int units = CG * 2 * g.nk;
-        for (int u = lt; landed && u < units; u += LT) {
-            const int co = u % CG, cib = u / CG;
-            const int k = cib >> 1, cb = cib & 1, ci0 = CU * cib;
-            const int nj = co < co_n ? (Cin - ci0 < CU ? Cin - ci0 : CU) : 0;   // real channels of this unit
-            const float *src = raw + (size_t)co * g.raw_pitch * 4 + (size_t)ci0 * RS;   // [j][rr][ss]
-            float f[CU * 9];   // [j][r][s] of the 3 x 3 taps
-            if (R == 3 && S == 3 && nj == CU) {
-#pragma unroll
-                for (int q = 0; q < CU * 9 / 4; ++q) {
-                    const float4 v = *reinterpret_cast<const float4 *>(src + 4 * q);
-                    f[4 * q] = v.x;
-                    f[4 * q + 1] = v.y;
-                    f[4 * q + 2] = v.z;
-                    f[4 * q + 3] = v.w;
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < CU; ++j)
-#pragma unroll
-                    for (int t = 0; t < 9; ++t) {
-                        const int rr = t / 3 - (3 - R) / 2, ss = t % 3 - (3 - S) / 2;
-                        f[j * 9 + t] = (j < nj && rr >= 0 && rr < R && ss >= 0 && ss < S) ? src[j * RS + rr * S + ss] : 0.f;
-                    }
-            }
-#pragma unroll
-            for (int t = 0; t < 9; ++t) {
-                const int r = t / 3, s = t % 3;
-                uint4 o;
-                if constexpr (CU == 4) {
-                    o = make_uint4(__float_as_uint(f[t]), __float_as_uint(f[9 + t]), __float_as_uint(f[18 + t]),
-                                   __float_as_uint(f[27 + t]));
-                } else {
-                    o = make_uint4(tc::pack_bf16(f[t], f[9 + t]), tc::pack_bf16(f[18 + t], f[27 + t]),
-                                   tc::pack_bf16(f[36 + t], f[45 + t]), tc::pack_bf16(f[54 + t], f[63 + t]));
-                }
-                bank[((k * 3 + r) * 2 + cb) * NB + s * CG + co] = o;
-            }
-        }
-        // B rows n >= 3 * CG (N rounded up to a multiple of 16) are zero
-        constexpr int PADN = NB - 3 * CG;
-        if constexpr (PADN > 0) {
-            for (int e = lt; e < g.nk * 3 * 2 * PADN; e += LT)
-                bank[(e / PADN) * NB + 3 * CG + e % PADN] = make_uint4(0u, 0u, 0u, 0u);
-        }
+        if (landed)
+            tc::stage_filter_bank<CG, OP>(reinterpret_cast<const float *>(raw_sm), reinterpret_cast<uint4 *>(wsm),
+                                          g.raw_pitch, co_n, Cin, R, S, g.nk, warp < 4 ? tid : tid - 32, LT);
         // the staged weights' buffers go to the TMA (async proxy) next, the
         // bank to the tensor core
         fence_proxy_async_smem();
@@ -658,7 +458,7 @@ static bool tc_geometry(int Cg, int NB, int kc, int rowb, int groups, int Cin, i
     double best_eff = 0;
     // the OIHW weights are staged in the stage buffers first: an odd pitch
     // of 16-byte units per output channel
-    const int raw_pitch = (Cin * RS / 4) | 1;
+    const int raw_pitch = tc::filter_raw_pitch(Cin, RS);
     const size_t raw = (size_t)Cg * raw_pitch * 16;
     for (int MT = 1; MT * NB <= tc::TMEM_BUF && MT <= 16; ++MT) {
         const int TR = 4 * MT;

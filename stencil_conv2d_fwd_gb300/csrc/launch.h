@@ -49,6 +49,16 @@ cudaError_t launch_transpose_batched(const float *src, float *dst, int N, long l
 // FP32 FMA rate probe (peak.cu).
 cudaError_t launch_ffma_peak(float *sink, int blocks, int iters, cudaStream_t st);
 
+// Two 3 x 3 layers fused on the tensor cores (conv_tc_fused.cu): x NHWC fp32
+// (C0 channels) -> act1(conv(x, w1) + b1) with C1 = 32 channels, kept on
+// chip -> y = act2(conv(., w2) + b2) NHWC fp32 with C2 <= 8 channels.
+struct FusedArgs {
+    const float *x, *w1, *b1, *w2, *b2;
+    float *y;
+    int N, H, W, C0, C1, C2, act1, act2;
+};
+cudaError_t launch_conv_tc_fused2(const FusedArgs &a, cudaStream_t st);
+
 // First-call autotuner (autotune.cu): whether sc_set_autotune turned it on,
 // and conv2d_fwd for NHWC tensors through it (3 x 3 filters, Cin > 1).
 bool autotune_enabled();
