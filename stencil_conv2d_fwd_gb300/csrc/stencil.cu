@@ -18,12 +18,16 @@
 //
 // Two ways to bring rows in:
 //  * stencil_tma_kernel (GB300 path): each warp streams its strip through a
-//    ring of 4 shared-memory slots of 4 rows x 136 columns (its 128 columns
+//    ring of 4 shared-memory slots of 5 rows x 136 columns (its 128 columns
 //    plus 4 on each side), filled by 2-D TMA copies (cp.async.bulk.tensor)
 //    that complete on one mbarrier per slot, so three slots' copies are in
-//    flight while the fourth is consumed.  Lanes read their 4 pixels and 2 + 2
-//    halo pixels from the slot.  Waits are bounded in time; on expiry the
-//    kernel records SC_ERR_DEVICE_TIMEOUT, drains its copies and returns.
+//    flight while the fourth is consumed.  Lanes read their 4 pixels from the
+//    slot and the 2 + 2 halo pixels from the neighbour lanes (shuffles).  A
+//    slot holds as many rows as the vertical window, so in a band away from
+//    the image's top and bottom edges the window's ring index of every row is
+//    a compile-time constant of the unrolled slot loop and no register moves.
+//    Waits are bounded in time; on expiry the kernel records
+//    SC_ERR_DEVICE_TIMEOUT, drains its copies and returns.
 //  * stencil_regs_kernel (any size or alignment): each lane loads its 4
 //    pixels; the halo pixels come from the neighbour lanes by shuffle.
 #include <cuda.h>
@@ -167,10 +171,13 @@ __global__ void __launch_bounds__(ST_NWARPS * 32)
 // ---------------------------------------------------------------------------
 static constexpr int TS_WARPS = 4;                 // warps per CTA
 static constexpr int TS_D = 4;                     // ring slots per warp
-static constexpr int TS_RB = 4;                    // rows per slot (TMA box height)
+static constexpr int TS_RB = 5;                    // rows per slot (TMA box height) = the vertical window
 static constexpr int TS_SW = 136;                  // columns per slot row: x0-4 .. x0+131
-static constexpr int TS_SLOT = TS_RB * TS_SW;      // floats per slot
+static constexpr int TS_SLOT = TS_RB * TS_SW;      // floats per slot (one TMA box)
 static constexpr unsigned TS_SLOT_BYTES = TS_SLOT * 4;
+// slots start 128-byte aligned (a TMA destination): the pitch rounds the box up
+static constexpr int TS_SLOT_PITCH = (TS_SLOT * 4 + 127) / 128 * 128 / 4;
+static_assert((TS_SLOT_PITCH * 4) % 128 == 0 && TS_SLOT_PITCH >= TS_SLOT, "TMA destinations must be 128-byte aligned");
 
 // Number of times input row yy occurs in the clamped row sequence
 // clamp(v, 0, H-1), v = y0-2 .. y1+1, that a band [y0, y1) consumes.
@@ -187,7 +194,7 @@ __global__ void __launch_bounds__(TS_WARPS * 32)
     stencil_tma_kernel(const __grid_constant__ CUtensorMap tm, float *__restrict__ out, int H, int W,
                        int band, int nstrips, int *status, unsigned long long timeout_ns, int drop_copy)
 {
-    __shared__ __align__(128) float ring[TS_WARPS][TS_D][TS_SLOT];
+    __shared__ __align__(128) float ring[TS_WARPS][TS_D][TS_SLOT_PITCH];
     __shared__ __align__(8) unsigned long long bars[TS_WARPS][TS_D];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -211,55 +218,119 @@ __global__ void __launch_bounds__(TS_WARPS * 32)
     auto issue = [&](int c) {  // lane 0: rows ys + 4c .. ys + 4c + 3 into slot c % D
         const int d = c % TS_D;
         mbar_arrive_expect_tx(bar0 + 8 * d, TS_SLOT_BYTES);
-        if (c != drop_copy) tma_load_2d(smem_u32(slots + d * TS_SLOT), &tm, xs - 4, ys + c * TS_RB, bar0 + 8 * d);
+        if (c != drop_copy) tma_load_2d(smem_u32(slots + d * TS_SLOT_PITCH), &tm, xs - 4, ys + c * TS_RB, bar0 + 8 * d);
     };
     if (lane == 0)
         for (int c = 0; c < min(TS_D, nchunks); ++c) issue(c);
 
     const int x0 = xs + 4 * lane;
-    float4 t[5], iv[3];
-    int nv = 0;
     int c = 0;
     bool failed = false;
-    for (; c < nchunks; ++c) {
-        const int d = c % TS_D;
-        if (!mbar_wait_bounded(bar0 + 8 * d, (c / TS_D) & 1, timeout_ns)) {
-            failed = true;
-            break;
-        }
-        const float *sl = slots + d * TS_SLOT;
-        for (int j = 0; j < TS_RB; ++j) {
-            const int yy = ys + c * TS_RB + j;
-            if (yy >= ye) break;
-            const float *rp = sl + j * TS_SW;
-            const float4 own = *reinterpret_cast<const float4 *>(rp + 4 + 4 * lane);
-            float2 lh = *reinterpret_cast<const float2 *>(rp + 2 + 4 * lane);
-            float2 rh = *reinterpret_cast<const float2 *>(rp + 8 + 4 * lane);
-            if (x0 == 0) lh = make_float2(own.x, own.x);          // columns -2, -1
-            if (x0 + 4 >= W) rh = make_float2(own.w, own.w);      // columns W, W+1 (W % 4 == 0)
-            Row8 r;
-            r.v[0] = lh.x; r.v[1] = lh.y; r.v[2] = own.x; r.v[3] = own.y;
-            r.v[4] = own.z; r.v[5] = own.w; r.v[6] = rh.x; r.v[7] = rh.y;
-            const float4 t1 = st_hblur(r);
-            for (int k = st_row_count(yy, y0, y1, H); k > 0; --k) {
-                t[0] = t[1]; t[1] = t[2]; t[2] = t[3]; t[3] = t[4]; t[4] = t1;
-                iv[0] = iv[1]; iv[1] = iv[2]; iv[2] = own;
-                if (++nv >= 5) {
-                    const int oy = y0 + nv - 5;
+    if (y0 >= 2 && y1 + 2 <= H) {
+        // Interior band (no row is clamped): input row i of the band (image
+        // row y0 - 2 + i) is row i % 5 of chunk i / 5, and its horizontal
+        // pass goes to ring register t[i % 5]; with 5-row chunks that index
+        // is the chunk-row index, a compile-time constant once the chunk is
+        // unrolled, so the window never moves.  Output row y0 + i - 4 uses
+        // t rows i - 4 .. i and input row i - 2 (iv[(i - 2) % 5]).
+        const int nrows = ye - ys;
+        float4 t[5], iv[5];
+        for (; c < nchunks; ++c) {
+            const int d = c % TS_D;
+            if (!mbar_wait_bounded(bar0 + 8 * d, (c / TS_D) & 1, timeout_ns)) {
+                failed = true;
+                break;
+            }
+            const float *sl = slots + d * TS_SLOT_PITCH;
+#pragma unroll
+            for (int j = 0; j < TS_RB; ++j) {
+                const int i = c * TS_RB + j;
+                if (i >= nrows) break;   // the same for the whole warp
+                const float *rp = sl + j * TS_SW;
+                const float4 own = *reinterpret_cast<const float4 *>(rp + 4 + 4 * lane);
+                // halo pixels from the neighbour lanes; the strip's outer two
+                // on each side from the slot; clamp at the image's edges
+                float l0 = __shfl_up_sync(0xffffffffu, own.z, 1), l1 = __shfl_up_sync(0xffffffffu, own.w, 1);
+                float r0 = __shfl_down_sync(0xffffffffu, own.x, 1), r1 = __shfl_down_sync(0xffffffffu, own.y, 1);
+                if (lane == 0) {
+                    const float2 h = *reinterpret_cast<const float2 *>(rp + 2);
+                    l0 = h.x;
+                    l1 = h.y;
+                }
+                if (lane == 31) {
+                    const float2 h = *reinterpret_cast<const float2 *>(rp + 4 + 4 * 32);
+                    r0 = h.x;
+                    r1 = h.y;
+                }
+                if (x0 == 0) l0 = l1 = own.x;             // columns -2, -1
+                if (x0 + 4 >= W) r0 = r1 = own.w;          // columns W, W + 1 (W % 4 == 0)
+                Row8 r;
+                r.v[0] = l0; r.v[1] = l1; r.v[2] = own.x; r.v[3] = own.y;
+                r.v[4] = own.z; r.v[5] = own.w; r.v[6] = r0; r.v[7] = r1;
+                t[j] = st_hblur(r);
+                iv[j] = own;
+                if (i >= 4) {
+                    const float4 &a = t[(j + 1) % 5], &b = t[(j + 2) % 5], &cc = t[(j + 3) % 5], &dd = t[(j + 4) % 5],
+                                 &e = t[j], &v = iv[(j + 3) % 5];
                     float4 o;
-                    o.x = st_unsharp(iv[0].x, st_vblur1(t[0].x, t[1].x, t[2].x, t[3].x, t[4].x));
-                    o.y = st_unsharp(iv[0].y, st_vblur1(t[0].y, t[1].y, t[2].y, t[3].y, t[4].y));
-                    o.z = st_unsharp(iv[0].z, st_vblur1(t[0].z, t[1].z, t[2].z, t[3].z, t[4].z));
-                    o.w = st_unsharp(iv[0].w, st_vblur1(t[0].w, t[1].w, t[2].w, t[3].w, t[4].w));
-                    if (x0 < W) stg_stream(reinterpret_cast<float4 *>(out + (long long)oy * W + x0), o);
+                    o.x = st_unsharp(v.x, st_vblur1(a.x, b.x, cc.x, dd.x, e.x));
+                    o.y = st_unsharp(v.y, st_vblur1(a.y, b.y, cc.y, dd.y, e.y));
+                    o.z = st_unsharp(v.z, st_vblur1(a.z, b.z, cc.z, dd.z, e.z));
+                    o.w = st_unsharp(v.w, st_vblur1(a.w, b.w, cc.w, dd.w, e.w));
+                    if (x0 < W) stg_stream(reinterpret_cast<float4 *>(out + (long long)(y0 + i - 4) * W + x0), o);
                 }
             }
+            // every lane is done reading slot d (its values fed the FMAs above)
+            __syncwarp();
+            if (lane == 0 && c + TS_D < nchunks) {
+                fence_proxy_async_smem();
+                issue(c + TS_D);
+            }
         }
-        // every lane is done reading slot d (its values fed the FMAs above)
-        __syncwarp();
-        if (lane == 0 && c + TS_D < nchunks) {
-            fence_proxy_async_smem();
-            issue(c + TS_D);
+    } else {
+        // A band at the top or bottom edge: clamped rows repeat, so each
+        // loaded row is consumed st_row_count times and the window shifts.
+        float4 t[5], iv[3];
+        int nv = 0;
+        for (; c < nchunks; ++c) {
+            const int d = c % TS_D;
+            if (!mbar_wait_bounded(bar0 + 8 * d, (c / TS_D) & 1, timeout_ns)) {
+                failed = true;
+                break;
+            }
+            const float *sl = slots + d * TS_SLOT_PITCH;
+            for (int j = 0; j < TS_RB; ++j) {
+                const int yy = ys + c * TS_RB + j;
+                if (yy >= ye) break;
+                const float *rp = sl + j * TS_SW;
+                const float4 own = *reinterpret_cast<const float4 *>(rp + 4 + 4 * lane);
+                float2 lh = *reinterpret_cast<const float2 *>(rp + 2 + 4 * lane);
+                float2 rh = *reinterpret_cast<const float2 *>(rp + 8 + 4 * lane);
+                if (x0 == 0) lh = make_float2(own.x, own.x);          // columns -2, -1
+                if (x0 + 4 >= W) rh = make_float2(own.w, own.w);      // columns W, W+1 (W % 4 == 0)
+                Row8 r;
+                r.v[0] = lh.x; r.v[1] = lh.y; r.v[2] = own.x; r.v[3] = own.y;
+                r.v[4] = own.z; r.v[5] = own.w; r.v[6] = rh.x; r.v[7] = rh.y;
+                const float4 t1 = st_hblur(r);
+                for (int k = st_row_count(yy, y0, y1, H); k > 0; --k) {
+                    t[0] = t[1]; t[1] = t[2]; t[2] = t[3]; t[3] = t[4]; t[4] = t1;
+                    iv[0] = iv[1]; iv[1] = iv[2]; iv[2] = own;
+                    if (++nv >= 5) {
+                        const int oy = y0 + nv - 5;
+                        float4 o;
+                        o.x = st_unsharp(iv[0].x, st_vblur1(t[0].x, t[1].x, t[2].x, t[3].x, t[4].x));
+                        o.y = st_unsharp(iv[0].y, st_vblur1(t[0].y, t[1].y, t[2].y, t[3].y, t[4].y));
+                        o.z = st_unsharp(iv[0].z, st_vblur1(t[0].z, t[1].z, t[2].z, t[3].z, t[4].z));
+                        o.w = st_unsharp(iv[0].w, st_vblur1(t[0].w, t[1].w, t[2].w, t[3].w, t[4].w));
+                        if (x0 < W) stg_stream(reinterpret_cast<float4 *>(out + (long long)oy * W + x0), o);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0 && c + TS_D < nchunks) {
+                fence_proxy_async_smem();
+                issue(c + TS_D);
+            }
         }
     }
     if (failed) {
