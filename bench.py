@@ -91,6 +91,9 @@ def kernel_sources(L):
     c = "stencil_conv2d_fwd_gb300/csrc/"
     if L.cin == 1:
         return [c + "conv_c1.cu", c + "common.cuh"]
+    if max(L.r, L.s) == 3:   # the TMA-staged kernel and the dispatch that picks it
+        return [c + "conv_tma.cuh", c + "conv_tma_k3.cu", c + "common.cuh", c + "conv_general_k3.cu",
+                c + "conv_general_k3n.cu"]
     return [c + "conv_general.cuh", c + "common.cuh", c + f"conv_general_k{max(L.r, L.s)}.cu"]
 
 

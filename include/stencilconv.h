@@ -22,6 +22,13 @@
 extern "C" {
 #endif
 
+/* The library is built with hidden symbol visibility: only the functions
+ * declared here are exported, so two copies of the library (or another
+ * library with the same internal names) can be loaded in one process. */
+#if defined(__GNUC__)
+#pragma GCC visibility push(default)
+#endif
+
 struct CUstream_st;                     /* = cudaStream_t's target type */
 typedef struct CUstream_st *sc_stream_t;
 
@@ -290,6 +297,10 @@ int sc_test_stencil_wait_expiry(const float *in, float *out, int H, int W, int d
 int conv2d_fwd_nchw_noalloc(const float *x, const float *w, const float *b, float *y,
                             int N, int H, int W, int Cin, int Cout, int R, int S,
                             int act, sc_stream_t stream);
+
+#if defined(__GNUC__)
+#pragma GCC visibility pop
+#endif
 
 #ifdef __cplusplus
 }

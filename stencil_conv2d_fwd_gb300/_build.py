@@ -20,7 +20,10 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libstencilconv.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
+# hidden visibility: only the C API of include/stencilconv.h is exported
+# (kernel stubs and the launchers' function-local statics stay private to
+# this copy of the library)
+FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden", "-Xptxas", "-v",
          "--expt-relaxed-constexpr", "-I", CSRC, "-I", INCLUDE]
 
 

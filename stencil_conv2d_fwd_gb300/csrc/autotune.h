@@ -16,4 +16,17 @@ struct TuneCand {
 // (conv_general_k3t.cu, conv_general_k3tn.cu).  Returns the count.
 int k3_candidates(const ConvArgs &a, const TuneCand **out);
 
+// TMA-staged configurations for 3 x 3 filters (conv_tma_k3.cu), named
+// F<output channels per CTA>, W<pixels per thread>, <tile rows>; "pc": FMAs
+// paired along input channels.
+cudaError_t k3_tma_f4_w5_h4_pc(const ConvArgs &a, cudaStream_t st);
+cudaError_t k3_tma_f4_w5_h4(const ConvArgs &a, cudaStream_t st);
+cudaError_t k3_tma_f4_w5_h8_pc(const ConvArgs &a, cudaStream_t st);
+cudaError_t k3_tma_f4_w3_h4_pc(const ConvArgs &a, cudaStream_t st);
+cudaError_t k3_tma_f8_w5_h4(const ConvArgs &a, cudaStream_t st);
+cudaError_t k3_tma_f16_w5_h4(const ConvArgs &a, cudaStream_t st);
+cudaError_t k3_tma_f32_w7_h8(const ConvArgs &a, cudaStream_t st);
+cudaError_t k3_tma_f32_w5_h8(const ConvArgs &a, cudaStream_t st);
+cudaError_t k3_tma_f64_w7_h8(const ConvArgs &a, cudaStream_t st);
+
 }  // namespace sc

@@ -37,6 +37,13 @@ SC_HD int swz_col(int row, int c, int log2_chunks_per_row)
     return (row ^ c) & mask;
 }
 
+// TMA swizzle of a staged pixel of c_sh fp32 channels (c_sh = 8, 16 or 32:
+// 32-, 64- or 128-byte pixels, copied with the TMA swizzle of that span, in
+// stage rows of a multiple of 8 pixels from a 1024-byte-aligned base): the
+// copy XORs address bits 4.. with bits 7.., so 16-byte chunk q of pixel p is
+// stored at chunk q ^ tma_swz_key(p, c_sh) of that pixel.
+SC_HD int tma_swz_key(int p, int c_sh) { return (p * c_sh / 32) & (c_sh / 4 - 1); }
+
 #if defined(__CUDACC__)
 
 // ---------------------------------------------------------------------------

@@ -24,10 +24,20 @@
 //
 // GB300 changes to the method:
 //  * The FMAs are issued as packed dual-FP32 FMAs (__ffma2_rn, sm_100 and
-//    later) on pairs of output channels: the two filter values come as one
-//    half of a 16-byte filter unit and the pixel value is used twice, so one
-//    instruction does two of the thread's FMAs.  Each component rounds like
-//    fmaf, so results equal the scalar-FMA kernel's.
+//    later), each component rounding like fmaf.  Both operands of such an
+//    FMA are register pairs, and the pairing axis is chosen by the thread's
+//    accumulator count:
+//    - many accumulators (F_T x W_T > 32): pairs of output channels.  The
+//      two filter values are one half of a 16-byte filter unit; the pixel
+//      value is used twice, which costs one register copy per value and is
+//      spread over the F_T / 2 channel pairs.
+//    - few accumulators (PAIRC): pairs of input channels.  Each output keeps
+//      two partial sums, over the even and over the odd input channels,
+//      added once at the end; the pixel pair is one half of a 16-byte pixel
+//      unit and the filter pair one half of a 16-byte unit of 4 input
+//      channels (the filter bank is staged as [ci/4][r][s][F_TB][4]), so no
+//      operand needs a copy.  With 4 output channels the copies of the other
+//      pairing were half as many instructions as the FMAs themselves.
 //  * Persistent CTAs: the grid is sized to the resident CTAs, and each CTA
 //    keeps its whole filter bank (all input channels, transposed to
 //    [ci][r][s][F_TB]) in shared memory for all the blocks it computes, when
@@ -68,6 +78,7 @@ struct GenCfg {
     // consecutive lanes conflict-free for every kernel size.
     static constexpr int SWZ_MASK = (W_T % 8 == 0) ? 7 : (W_T % 4 == 0) ? 3 : (W_T % 2 == 0) ? 1 : 0;
     static constexpr int F_T = F_TB >= 8 ? 8 : 4;       // output channels per thread
+    static constexpr bool PAIRC = F_T * W_T_ <= 32;       // FMA pairs along input channels
     static constexpr int NG = F_T / 4;                   // float4 groups per thread
     static constexpr int T_X = F_TB / F_T;               // lanes along output channels
     static constexpr int PXL = 32 / T_X;                 // lanes along pixels
@@ -110,10 +121,13 @@ __host__ __device__ __forceinline__ int phys_col(int col)
     return (col & ~7) | ((col ^ ((col >> 3) & C::SWZ_MASK)) & 7);
 }
 
-// Copy filters for input channels [c0, c0 + nci) into ws[(ci-c0)*KK + r*K + s][F_TB]
-// (transposed, output channels contiguous), zero where the R x S filter has
-// no tap, where co >= Cout or ci >= Cin.  Lanes run along output channels,
-// so the shared-memory side is contiguous.
+// Copy filters for input channels [c0, c0 + nci) into shared memory, zero
+// where the R x S filter has no tap, where co >= Cout or ci >= Cin:
+//  * channel pairing: ws[(ci-c0)*KK + r*K + s][F_TB] (transposed, output
+//    channels contiguous);
+//  * PAIRC: ws[((ci-c0)/4)*KK + r*K + s][F_TB][4] (4 consecutive input
+//    channels of one output channel and tap contiguous).
+// Consecutive threads write consecutive shared-memory words.
 template <class C>
 __device__ __forceinline__ void gen_issue_filters(float *ws, const float *__restrict__ w, int co0,
                                                   int c0, int nci, int Cin, int Cout, int R, int S,
@@ -122,10 +136,18 @@ __device__ __forceinline__ void gen_issue_filters(float *ws, const float *__rest
     const int n = nci * C::KK * C::F_TB;
     const int dr = (C::K - R) / 2, ds = (C::K - S) / 2;
     for (int e = tid; e < n; e += C::NT) {
-        const int col = e % C::F_TB;
-        const int row = e / C::F_TB;
-        const int ci = c0 + row / C::KK;
-        const int rs = row % C::KK;
+        int col, ci, rs;
+        if constexpr (C::PAIRC) {
+            col = (e >> 2) % C::F_TB;
+            const int t = e / (4 * C::F_TB);
+            rs = t % C::KK;
+            ci = c0 + (t / C::KK) * 4 + (e & 3);
+        } else {
+            col = e % C::F_TB;
+            const int row = e / C::F_TB;
+            ci = c0 + row / C::KK;
+            rs = row % C::KK;
+        }
         const int r = rs / C::K - dr;
         const int s = rs % C::K - ds;
         const int co = co0 + col;
@@ -219,12 +241,21 @@ __global__ void __launch_bounds__(C::NT, C::MINB)
     cp_async_commit();
 
     int it = 0;
+    // accumulators: channel pairing uses acc, PAIRC the (even, odd input
+    // channel) partial sums acc2
+    constexpr int AF = C::PAIRC ? 1 : C::F_T, AW = C::PAIRC ? 1 : C::W_T;
+    constexpr int PF = C::PAIRC ? C::F_T : 1, PW = C::PAIRC ? C::W_T : 1;
     for (; tile < ntiles; tile += gridDim.x) {
-        float acc[C::F_T][C::W_T];
+        float acc[AF][AW];
+        float2 acc2[PF][PW];
 #pragma unroll
-        for (int f = 0; f < C::F_T; ++f)
+        for (int f = 0; f < AF; ++f)
 #pragma unroll
-            for (int j = 0; j < C::W_T; ++j) acc[f][j] = 0.0f;
+            for (int j = 0; j < AW; ++j) acc[f][j] = 0.0f;
+#pragma unroll
+        for (int f = 0; f < PF; ++f)
+#pragma unroll
+            for (int j = 0; j < PW; ++j) acc2[f][j] = make_float2(0.0f, 0.0f);
 
         for (int k = 0; k < nk; ++k, ++it) {
             // prefetch the next step: the next channel chunk, or the first
@@ -245,6 +276,44 @@ __global__ void __launch_bounds__(C::NT, C::MINB)
             const float4 *w_s4 =
                 C::RESIDENT ? reinterpret_cast<const float4 *>(w_res) + (size_t)k * C::C_SH * C::KK * (C::F_TB / 4)
                             : reinterpret_cast<const float4 *>(st + C::IN_CHUNKS * 4);
+            if constexpr (C::PAIRC) {
+                // the whole step unrolled: every shared-memory address is a
+                // per-lane base plus a constant
+#pragma unroll
+                for (int cb = 0; cb < C::CB; ++cb) {
+#pragma unroll
+                    for (int r = 0; r < C::K; ++r) {
+                        // one input row: W_T + K - 1 pixels x 4 channels
+                        const float4 *row = in_s + cb * C::PLANE + (ry + r) * C::TWP;
+                        float4 px[C::WIN];
+#pragma unroll
+                        for (int j = 0; j < C::WIN; ++j) px[j] = row[pcol[j]];
+                        // filter units ((cb * K + r) * K + s) * F_TB + co, 4 input channels each
+                        const float4 *wr = w_s4 + (cb * C::KK + r * C::K) * C::F_TB + 4 * tx;
+#pragma unroll
+                        for (int s = 0; s < C::K; ++s) {
+                            float4 wv[C::F_T];
+#pragma unroll
+                            for (int g = 0; g < C::NG; ++g)
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) wv[4 * g + e] = wr[s * C::F_TB + g * (C::F_TB / C::NG) + e];
+                            // input channels 0, 1 of the unit, then 2, 3
+#pragma unroll
+                            for (int j = 0; j < C::W_T; ++j)
+#pragma unroll
+                                for (int f = 0; f < C::F_T; ++f)
+                                    acc2[f][j] = __ffma2_rn(make_float2(wv[f].x, wv[f].y),
+                                                            make_float2(px[j + s].x, px[j + s].y), acc2[f][j]);
+#pragma unroll
+                            for (int j = 0; j < C::W_T; ++j)
+#pragma unroll
+                                for (int f = 0; f < C::F_T; ++f)
+                                    acc2[f][j] = __ffma2_rn(make_float2(wv[f].z, wv[f].w),
+                                                            make_float2(px[j + s].z, px[j + s].w), acc2[f][j]);
+                        }
+                    }
+                }
+            } else {
 #pragma unroll 1
             for (int cb = 0; cb < C::CB; ++cb) {
 #pragma unroll 1
@@ -288,8 +357,13 @@ __global__ void __launch_bounds__(C::NT, C::MINB)
                     }
                 }
             }
+            }
             __syncthreads();
         }
+        auto res = [&](int f, int j) {
+            if constexpr (C::PAIRC) return acc2[f][j].x + acc2[f][j].y;
+            else return acc[f][j];
+        };
 
         // epilogue: bias, activation, 16-byte NHWC stores of 4 output channels
         int n, y0, x0;
@@ -305,10 +379,10 @@ __global__ void __launch_bounds__(C::NT, C::MINB)
                         const int gx = x0 + cx0 + j;
                         if (gx < W) {
                             float4 o;
-                            o.x = relu_if(acc[4 * g + 0][j] + bv[4 * g + 0], act);
-                            o.y = relu_if(acc[4 * g + 1][j] + bv[4 * g + 1], act);
-                            o.z = relu_if(acc[4 * g + 2][j] + bv[4 * g + 2], act);
-                            o.w = relu_if(acc[4 * g + 3][j] + bv[4 * g + 3], act);
+                            o.x = relu_if(res(4 * g + 0, j) + bv[4 * g + 0], act);
+                            o.y = relu_if(res(4 * g + 1, j) + bv[4 * g + 1], act);
+                            o.z = relu_if(res(4 * g + 2, j) + bv[4 * g + 2], act);
+                            o.w = relu_if(res(4 * g + 3, j) + bv[4 * g + 3], act);
                             *reinterpret_cast<float4 *>(y + ((((long long)n * H + gy) * W + gx) * Cout + co)) = o;
                         }
                     }

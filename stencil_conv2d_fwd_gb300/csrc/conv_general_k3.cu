@@ -1,13 +1,17 @@
-// Instantiations of the general direct convolution for kernel size K = 3,
-// more than 16 output channels (conv_general_k3n.cu has the rest).
+// Direct convolution for kernel size K = 3, more than 16 output channels
+// (conv_general_k3n.cu has the rest).
 #include "conv_general.cuh"
 
 namespace sc {
 cudaError_t launch_conv_general_k3_narrow(const ConvArgs &a, cudaStream_t st);
 
+// The TMA-staged kernel (conv_tma_k3.cu) first; the cp.async-staged
+// configurations where it does not apply (filter banks above its limit).
 cudaError_t launch_conv_general_k3(const ConvArgs &a, cudaStream_t st)
 {
     if (a.Cout <= 16) return launch_conv_general_k3_narrow(a, st);
+    const cudaError_t e = launch_conv_tma_k3_wide(a, st);
+    if (e != cudaErrorNotSupported) return e;
     if (a.Cin % 16 == 0) return dispatch_wide<3, 16>(a, st);
     return dispatch_wide<3, 8>(a, st);
 }

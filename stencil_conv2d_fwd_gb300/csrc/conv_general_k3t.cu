@@ -30,6 +30,7 @@ static const TuneCand k3_wide64[] = {
     {"F64 W8 8x32", k3_wide_w8_f64},
     {"F64 W8 4x32 2/SM", cand<64, 8, 4, 32, 16, 2>},
     {"F64 W7 4x28 2/SM", cand<64, 7, 4, 28, 16, 2>},
+    {"TMA F64 W7 8x28", k3_tma_f64_w7_h8},
 };
 static const TuneCand k3_wide32[] = {
     {"heuristic", launch_conv_general_k3},
@@ -37,6 +38,8 @@ static const TuneCand k3_wide32[] = {
     {"F32 W8 8x64", k3_wide_w8_f32},
     {"F32 W8 4x64 2/SM", cand<32, 8, 4, 64, 16, 2>},
     {"F32 W4 8x32", cand<32, 4, 8, 32, 16, 1>},
+    {"TMA F32 W7 8x56", k3_tma_f32_w7_h8},
+    {"TMA F32 W5 8x40", k3_tma_f32_w5_h8},
 };
 static const TuneCand k3_only_heuristic[] = {{"heuristic", launch_conv_general_k3}};
 

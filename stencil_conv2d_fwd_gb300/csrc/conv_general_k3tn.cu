@@ -19,16 +19,22 @@ static const TuneCand k3_n16[] = {
     {"heuristic", launch_conv_general_k3},
     {"F16 W8 4x128", cand_n<16, 8, 4, 128, 2>},
     {"F16 W4 8x64", cand_n<16, 4, 8, 64, 1>},
+    {"TMA F16 W5 4x80", k3_tma_f16_w5_h4},
 };
 static const TuneCand k3_n8[] = {
     {"heuristic", launch_conv_general_k3},
     {"F8 W8 4x256", cand_n<8, 8, 4, 256, 2>},
+    {"TMA F8 W5 4x160", k3_tma_f8_w5_h4},
 };
 static const TuneCand k3_n4[] = {
     {"heuristic", launch_conv_general_k3},
     {"F4 W8 4x256", cand_n<4, 8, 4, 256, 2>},
     {"F4 W4 2x128 4/SM", cand_n<4, 4, 2, 128, 4>},
     {"F4 W8 2x256 4/SM", cand_n<4, 8, 2, 256, 4>},
+    {"TMA F4 W5 4x160 pc", k3_tma_f4_w5_h4_pc},
+    {"TMA F4 W5 4x160", k3_tma_f4_w5_h4},
+    {"TMA F4 W5 8x160 pc", k3_tma_f4_w5_h8_pc},
+    {"TMA F4 W3 4x96 pc", k3_tma_f4_w3_h4_pc},
 };
 
 const TuneCand *k3_narrow_table(const ConvArgs &a, int *n)

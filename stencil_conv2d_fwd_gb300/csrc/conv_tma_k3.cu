@@ -1,0 +1,83 @@
+// Instantiations of the TMA-staged direct convolution (conv_tma.cuh) for
+// 3 x 3 filters and 16 or fewer output channels, and the driver's
+// tensor-map encoder they share.
+#include <mutex>
+
+#include "autotune.h"
+#include "conv_tma.cuh"
+
+namespace sc {
+
+PFN_cuTensorMapEncodeTiled_v12000 conv_tma_encoder()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// <K, F_TB, W_T, TH, C_SH, NSTAGE, MINB, PAIRC>
+cudaError_t k3_tma_f4_w5_h4_pc(const ConvArgs &a, cudaStream_t st)
+{
+    return launch_conv_tma<TmaCfg<3, 4, 5, 4, 8, 3, 2, true>>(a, st);
+}
+cudaError_t k3_tma_f4_w5_h4(const ConvArgs &a, cudaStream_t st)
+{
+    return launch_conv_tma<TmaCfg<3, 4, 5, 4, 8, 3, 2, false>>(a, st);
+}
+cudaError_t k3_tma_f4_w5_h8_pc(const ConvArgs &a, cudaStream_t st)
+{
+    return launch_conv_tma<TmaCfg<3, 4, 5, 8, 8, 3, 1, true>>(a, st);
+}
+cudaError_t k3_tma_f4_w3_h4_pc(const ConvArgs &a, cudaStream_t st)
+{
+    return launch_conv_tma<TmaCfg<3, 4, 3, 4, 8, 3, 3, true>>(a, st);
+}
+cudaError_t k3_tma_f8_w5_h4(const ConvArgs &a, cudaStream_t st)
+{
+    return launch_conv_tma<TmaCfg<3, 8, 5, 4, 8, 3, 2, false>>(a, st);
+}
+cudaError_t k3_tma_f16_w5_h4(const ConvArgs &a, cudaStream_t st)
+{
+    return launch_conv_tma<TmaCfg<3, 16, 5, 4, 8, 3, 2, false>>(a, st);
+}
+cudaError_t k3_tma_f32_w7_h8(const ConvArgs &a, cudaStream_t st)
+{
+    return launch_conv_tma<TmaCfg<3, 32, 7, 8, 8, 3, 1, false>>(a, st);
+}
+cudaError_t k3_tma_f32_w5_h8(const ConvArgs &a, cudaStream_t st)
+{
+    return launch_conv_tma<TmaCfg<3, 32, 5, 8, 8, 3, 1, false>>(a, st);
+}
+cudaError_t k3_tma_f64_w7_h8(const ConvArgs &a, cudaStream_t st)
+{
+    return launch_conv_tma<TmaCfg<3, 64, 7, 8, 8, 3, 1, false>>(a, st);
+}
+
+// Default for more than 16 output channels: 64 per CTA above 32, else 32
+// with the pixel run (5 or 7) that leaves fewer columns past the image edge.
+cudaError_t launch_conv_tma_k3_wide(const ConvArgs &a, cudaStream_t st)
+{
+    if (a.Cout > 32) return k3_tma_f64_w7_h8(a, st);
+    const int waste40 = (a.W + 39) / 40 * 40 - a.W, waste56 = (a.W + 55) / 56 * 56 - a.W;
+    return waste56 < waste40 ? k3_tma_f32_w7_h8(a, st) : k3_tma_f32_w5_h8(a, st);
+}
+
+// Default for 16 or fewer output channels: the TMA-staged kernel, one
+// output-channel group per CTA; cudaErrorNotSupported where it does not
+// apply (the caller then uses conv_general_k3n.cu's configurations).
+cudaError_t launch_conv_tma_k3_narrow(const ConvArgs &a, cudaStream_t st)
+{
+    if (a.Cout <= 4) return k3_tma_f4_w5_h4(a, st);
+    if (a.Cout <= 8) return k3_tma_f8_w5_h4(a, st);
+    return k3_tma_f16_w5_h4(a, st);
+}
+
+}  // namespace sc

@@ -21,6 +21,12 @@ cudaError_t launch_conv_general_k3(const ConvArgs &a, cudaStream_t st);
 cudaError_t launch_conv_general_k5(const ConvArgs &a, cudaStream_t st);
 cudaError_t launch_conv_general_k7(const ConvArgs &a, cudaStream_t st);
 
+// TMA-staged direct convolution for 3 x 3 filters (conv_tma_k3.cu), 16 or
+// fewer output channels (narrow) or more (wide); cudaErrorNotSupported
+// where it does not apply.
+cudaError_t launch_conv_tma_k3_narrow(const ConvArgs &a, cudaStream_t st);
+cudaError_t launch_conv_tma_k3_wide(const ConvArgs &a, cudaStream_t st);
+
 // NHWC convolution: picks the single-input-channel kernel or the general
 // kernel for K = max(R, S) (api.cu).
 cudaError_t launch_conv_nhwc(const ConvArgs &a, cudaStream_t st);

@@ -77,6 +77,35 @@ def test_every_candidate_matches_the_oracle(oracle_mod, cuda_dev, sc, shape):
     assert rc == sc.SC_ERR_UNSUPPORTED
 
 
+TMA_EDGES = [
+    # (N, Cin, Cout, H, W): TMA-staged candidates at their edges
+    (2, 12, 4, 7, 165),     # Cin % 8 != 0 (zero-filled channels), batch of 2, ragged tiles
+    (1, 4, 8, 5, 9),        # a single 4-channel step, image narrower than one tile
+    (1, 64, 16, 6, 81),     # 8 steps per tile, two output-channel lanes per pixel
+    (3, 20, 4, 3, 161),     # image shorter than one tile
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("shape", TMA_EDGES, ids=[str(s) for s in TMA_EDGES])
+def test_tma_candidates_at_their_edges(oracle_mod, cuda_dev, sc, shape):
+    N, Cin, Cout, H, W = shape
+    c = S.conv_case(970 + Cin + Cout + W, N, Cin, Cout, H, W, 3, 3, act=0)
+    L = c.layers[0]
+    yr, a = oracle_mod.conv2d_nchw(c.x, L.w, L.b, L.act)
+    names = sc.sc_autotune_candidates(Cin, Cout, 3, 3)
+    ran = 0
+    for i, name in enumerate(names):
+        if not name.startswith("TMA"):
+            continue
+        rc, y = _run_candidate(c.x, L.w, L.b, L.act, i, cuda_dev)
+        assert rc == sc.SC_OK, (name, sc.sc_status_string(rc))
+        assert_conv_close(y, yr, a, what=f"candidate {i} ({name}) {shape}")
+        ran += 1
+    assert ran >= 1
+    assert sc.sc_last_device_status() == sc.SC_OK
+
+
 @pytest.mark.gpu
 def test_tuned_call_caches_its_choice_and_repeats(oracle_mod, cuda_dev, sc):
     N, Cin, Cout, H, W = 1, 32, 32, 23, 97

@@ -24,12 +24,14 @@ def swz(tmp_path_factory):
     src = d / "swz.cpp"
     src.write_text(f'#include "{HDR}"\n'
                    'extern "C" int h_swz16(int i, int L) { return sc::swz16(i, L); }\n'
-                   'extern "C" int h_swz_col(int r, int c, int L) { return sc::swz_col(r, c, L); }\n')
+                   'extern "C" int h_swz_col(int r, int c, int L) { return sc::swz_col(r, c, L); }\n'
+                   'extern "C" int h_tma_key(int p, int c) { return sc::tma_swz_key(p, c); }\n')
     so = d / "libswz.so"
     subprocess.run(["g++", "-std=c++17", "-O1", "-fPIC", "-shared", str(src), "-o", str(so)], check=True)
     lib = ctypes.CDLL(str(so))
     lib.h_swz16.argtypes = [ctypes.c_int, ctypes.c_int]
     lib.h_swz_col.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    lib.h_tma_key.argtypes = [ctypes.c_int, ctypes.c_int]
     return lib
 
 
@@ -177,3 +179,62 @@ def test_transpose_tile_conflict_free(swz):
         assert bank_ways_32bit(words) == 1
         plain = [tx * 32 + rb for tx in range(32)]
         assert bank_ways_32bit(plain) == 32
+
+
+# ---------------------------------------------------------------------------
+# conv_tma.cuh: stages written by TMA copies with the swizzle of the staged
+# pixel's span (32, 64 or 128 bytes).  The copy XORs the 16-byte chunk bits
+# (4 and up) of each shared-memory address with the bits 7 and up, as many as
+# the span has chunk bits; stage rows are a multiple of 8 pixels and stages
+# are 1024-byte aligned.
+
+def tma_swizzled_byte(addr, span):
+    """Where a swizzled TMA copy puts the byte that an unswizzled copy would
+    put at `addr` (relative to a 1024-byte-aligned stage)."""
+    mask = span // 16 - 1
+    return addr ^ (((addr >> 7) & mask) << 4)
+
+
+@pytest.mark.parametrize("c_sh", [8, 16, 32])
+def test_tma_key_is_the_copy_swizzle(swz, c_sh):
+    span = 4 * c_sh
+    for row_pitch_px in (8, 16, 104, 168):            # stage rows: multiples of 8 pixels
+        for row in range(3):
+            for p in range(row_pitch_px):
+                base = (row * row_pitch_px + p) * span
+                for q in range(span // 16):
+                    want = tma_swizzled_byte(base + 16 * q, span)
+                    got = base + 16 * (q ^ swz.h_tma_key(p, c_sh))
+                    assert got == want
+
+
+# (F_TB, W_T, C_SH): the configurations conv_tma_k3.cu instantiates
+TMA_CFGS = [(4, 5, 8), (4, 3, 8), (8, 5, 8), (16, 5, 8), (32, 7, 8), (32, 5, 8), (64, 7, 8), (4, 5, 16)]
+
+
+@pytest.mark.parametrize("cfg", TMA_CFGS, ids=[f"F{a}_W{b}_C{c}" for a, b, c in TMA_CFGS])
+def test_tma_stage_pixel_reads_conflict_free(swz, cfg):
+    """conv_tma_kernel's pixel loads: lane -> (tx = lane % T_X, pixel lane
+    pl = lane / T_X), pixel pl * W_T + j of a tile row, 16-byte chunk cb.
+    Every 8-lane phase reads distinct chunks in distinct bank groups, and a
+    pixel's chunks are a permutation of its span."""
+    F_TB, W_T, C_SH = cfg
+    F_T = 8 if F_TB >= 8 else 4
+    T_X = F_TB // F_T
+    CB, PXB = C_SH // 4, 4 * C_SH
+    for j in range(W_T + 2):
+        for cb in range(CB):
+            chunks = []
+            for lane in range(32):
+                p = (lane // T_X) * W_T + j
+                chunks.append((p * PXB + 16 * (cb ^ swz.h_tma_key(p, C_SH))) // 16)
+            assert phases_conflict_free(chunks)
+    for p in range(64):
+        assert sorted(cb ^ swz.h_tma_key(p, C_SH) for cb in range(CB)) == list(range(CB))
+
+
+def test_tma_even_pixel_run_would_conflict(swz):
+    """With an even run (W_T = 4) the lanes of a phase read pixels 4 apart,
+    which the swizzle cannot separate: the kernel uses odd runs."""
+    chunks = [((lane * 4) * 32 + 16 * (0 ^ swz.h_tma_key(lane * 4, 8))) // 16 for lane in range(32)]
+    assert not phases_conflict_free(chunks)
