@@ -280,6 +280,175 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// The same computation for W % 4 == 0 and 16-byte aligned x and y (every
+// thread's 4 pixels are all inside or all outside the image), without the
+// per-row window shift: the K window rows live in a ring of registers, and
+// the row loop is unrolled K times so that the ring slot of every window row
+// is a compile-time constant (input row q of the band sits in slot q mod K).
+// Each input row is fetched two output rows before its first use (the rows
+// of all warps of an SM otherwise wait on the same fetch latency together).
+// The accumulators start at the bias (the sum's first term instead of its
+// last; the rounding stays within the FP32 bound), read from shared memory
+// with the filters, and the stores need one in-image test per thread.
+template <int K, int F_T, int CL>
+__global__ void __launch_bounds__(256, (K >= 7 && F_T >= 8) ? 1 : 2)
+    conv_c1_ring_kernel(const float *__restrict__ x, const float *__restrict__ w,
+                        const float *__restrict__ bias, float *__restrict__ y, int N, int H, int W,
+                        int Cout, int R, int S, int act, int rows_per_cta, int col_tiles)
+{
+    using C = C1Cfg<K, F_T, CL>;
+    __shared__ __align__(16) float ws[K * K * C::CO_CTA];
+    __shared__ __align__(16) float bs[C::CO_CTA];
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const int cl = lane % CL;
+    const int pl = lane / CL;
+    const int co0 = blockIdx.y * C::CO_CTA;
+    const int n = blockIdx.z;
+    const int ct = blockIdx.x % col_tiles;
+    const int rt = blockIdx.x / col_tiles;
+    const int x0 = (ct * nwarps + warp) * (C::PL * 4) + pl * 4;
+    const int y0 = rt * rows_per_cta;
+    const int y1 = min(H, y0 + rows_per_cta);
+    const bool px_ok = x0 < W;   // W % 4 == 0: all 4 pixels or none
+
+    for (int e = tid; e < K * K * C::CO_CTA; e += blockDim.x) {
+        const int col = e % C::CO_CTA;
+        const int tap = e / C::CO_CTA;
+        const int r = tap / K - (K - R) / 2;
+        const int s = tap % K - (K - S) / 2;
+        const int co = co0 + col;
+        float v = 0.f;
+        if (r >= 0 && r < R && s >= 0 && s < S && co < Cout) v = w[((long long)co * R + r) * S + s];
+        ws[e] = v;
+    }
+    for (int e = tid; e < C::CO_CTA; e += blockDim.x) bs[e] = (bias && co0 + e < Cout) ? bias[co0 + e] : 0.f;
+    __syncthreads();
+
+    const float *xn = x + (long long)n * H * W;
+    auto issue = [&](C1Raw &raw, int yy) {   // image row yy (zeros outside the image)
+        const bool ok = yy >= 0 && yy < H;
+        c1_issue_row<C>(raw, xn + (long long)(ok ? yy : 0) * W, ok, x0, W, true, pl);
+    };
+    float win[K][C::WIN];
+    // prologue: band rows q = 0 .. K - 2 (image rows y0 - HALO + q) into
+    // slots q, all fetches in flight together; row K - 1 stays in flight
+    C1Raw raw_c;   // band row i + K - 1, fetched during row i - 1
+    {
+        C1Raw pro[K > 1 ? K - 1 : 1];
+#pragma unroll
+        for (int t = 0; t < K - 1; ++t) issue(pro[t], y0 - C::HALO + t);
+        issue(raw_c, y0 + C::HALO);
+#pragma unroll
+        for (int t = 0; t < K - 1; ++t) c1_finish_row<C>(win[t], pro[t], pl, lane);
+    }
+
+    const int nrows = y1 - y0;
+    for (int m = 0; m < nrows; m += K) {
+#pragma unroll
+        for (int u = 0; u < K; ++u) {
+            const int i = m + u;
+            if (i < nrows) {   // the same for the whole CTA
+            // one output row at a time: keeps the unrolled rows from
+            // overlapping (their registers would not fit)
+            asm volatile("" ::: "memory");
+            const int oy = y0 + i;
+            C1Raw raw_n;   // band row i + K (image row oy + HALO + 1)
+            issue(raw_n, oy + C::HALO + 1);
+            float acc[F_T][4];
+            if constexpr (F_T >= 4) {
+#pragma unroll
+                for (int g = 0; g < F_T / 4; ++g) {
+                    const float4 b4 = *reinterpret_cast<const float4 *>(bs + g * 4 * CL + 4 * cl);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        acc[4 * g + 0][j] = b4.x;
+                        acc[4 * g + 1][j] = b4.y;
+                        acc[4 * g + 2][j] = b4.z;
+                        acc[4 * g + 3][j] = b4.w;
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int f = 0; f < F_T; ++f)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[f][j] = bs[cl * F_T + f];
+            }
+#pragma unroll
+            for (int ky = 0; ky < K; ++ky) {
+                float(&wr)[C::WIN] = win[(u + ky) % K];   // band row i + ky
+                if (ky == K - 1) c1_finish_row<C>(wr, raw_c, pl, lane);
+                asm volatile("" ::: "memory");
+#pragma unroll
+                for (int kx = 0; kx < K; ++kx) {
+                    const float *wt = ws + (ky * K + kx) * C::CO_CTA;
+                    float wv[F_T];
+                    if constexpr (F_T >= 4) {
+#pragma unroll
+                        for (int g = 0; g < F_T / 4; ++g) {
+                            const float4 t = *reinterpret_cast<const float4 *>(wt + g * 4 * CL + 4 * cl);
+                            wv[4 * g + 0] = t.x;
+                            wv[4 * g + 1] = t.y;
+                            wv[4 * g + 2] = t.z;
+                            wv[4 * g + 3] = t.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int f = 0; f < F_T; ++f) wv[f] = wt[cl * F_T + f];
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float v = wr[j + kx];
+                        if constexpr (F_T % 2 == 0) {
+                            const float2 vv = make_float2(v, v);
+#pragma unroll
+                            for (int f = 0; f < F_T; f += 2) {
+                                float2 a2 = make_float2(acc[f][j], acc[f + 1][j]);
+                                a2 = __ffma2_rn(make_float2(wv[f], wv[f + 1]), vv, a2);
+                                acc[f][j] = a2.x;
+                                acc[f + 1][j] = a2.y;
+                            }
+                        } else {
+#pragma unroll
+                            for (int f = 0; f < F_T; ++f) acc[f][j] = fmaf(wv[f], v, acc[f][j]);
+                        }
+                    }
+                }
+            }
+            raw_c = raw_n;
+            if (px_ok) {
+                float *yrow = y + ((long long)n * H + oy) * W * Cout;
+                if constexpr (F_T >= 4) {
+#pragma unroll
+                    for (int g = 0; g < F_T / 4; ++g) {
+                        const int co = co0 + g * 4 * CL + 4 * cl;
+                        if (co < Cout) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                float4 o;
+                                o.x = relu_if(acc[4 * g + 0][j], act);
+                                o.y = relu_if(acc[4 * g + 1][j], act);
+                                o.z = relu_if(acc[4 * g + 2][j], act);
+                                o.w = relu_if(acc[4 * g + 3][j], act);
+                                *reinterpret_cast<float4 *>(yrow + (long long)(x0 + j) * Cout + co) = o;
+                            }
+                        }
+                    }
+                } else if (co0 + cl < Cout) {
+                    // F_T == 1 (Cout == 1): four contiguous pixels of one channel
+                    *reinterpret_cast<float4 *>(yrow + x0) =
+                        make_float4(relu_if(acc[0][0], act), relu_if(acc[0][1], act), relu_if(acc[0][2], act),
+                                    relu_if(acc[0][3], act));
+                }
+            }
+            }
+        }
+    }
+}
+
 template <int K, int F_T, int CL>
 static cudaError_t launch_c1_cfg(const ConvArgs &a, cudaStream_t st)
 {
@@ -303,8 +472,14 @@ static cudaError_t launch_c1_cfg(const ConvArgs &a, cudaStream_t st)
     if (nb > 0x7fffffffLL || groups > 65535 || a.N > 65535) return cudaErrorInvalidConfiguration;
     const int vec = ((a.W & 3) == 0) && ((reinterpret_cast<uintptr_t>(a.x) & 15) == 0) &&
                     ((reinterpret_cast<uintptr_t>(a.y) & 15) == 0);
-    conv_c1_kernel<K, F_T, CL><<<dim3((unsigned)nb, groups, a.N), nwarps * 32, 0, st>>>(
-        a.x, a.w, a.b, a.y, a.N, a.H, a.W, a.Cout, a.R, a.S, a.act, rows_per_cta, col_tiles, vec);
+    // the ring needs more registers than 7 x 7 filters with 8 channels per
+    // thread leave at 2 CTAs per SM; those keep the shifting window
+    if (vec && !(K >= 7 && F_T >= 8))
+        conv_c1_ring_kernel<K, F_T, CL><<<dim3((unsigned)nb, groups, a.N), nwarps * 32, 0, st>>>(
+            a.x, a.w, a.b, a.y, a.N, a.H, a.W, a.Cout, a.R, a.S, a.act, rows_per_cta, col_tiles);
+    else
+        conv_c1_kernel<K, F_T, CL><<<dim3((unsigned)nb, groups, a.N), nwarps * 32, 0, st>>>(
+            a.x, a.w, a.b, a.y, a.N, a.H, a.W, a.Cout, a.R, a.S, a.act, rows_per_cta, col_tiles, vec);
     return cudaGetLastError();
 }
 

@@ -93,6 +93,9 @@ C1_SHAPES = [
     (1, 4, 20, 33, 5, 5), (1, 8, 31, 130, 5, 5), (1, 12, 9, 17, 3, 3), (1, 16, 40, 70, 7, 7),
     (1, 24, 16, 100, 5, 5), (1, 32, 50, 260, 5, 5), (2, 32, 23, 41, 3, 3), (1, 64, 12, 66, 5, 5),
     (1, 32, 10, 35, 1, 1), (1, 8, 15, 21, 3, 7), (1, 1, 64, 1030, 7, 7), (1, 32, 6, 1300, 5, 5),
+    # W % 4 == 0 (the register-ring kernel): every filter size, bands that are
+    # not a multiple of K rows, a 2-pixel-wide strip per lane group
+    (1, 32, 17, 96, 7, 7), (1, 8, 9, 44, 1, 1), (2, 16, 13, 52, 3, 3), (1, 4, 7, 8, 3, 5), (1, 1, 23, 36, 5, 5),
 ]
 
 
