@@ -17,12 +17,13 @@ struct TuneCand {
 int k3_candidates(const ConvArgs &a, const TuneCand **out);
 
 // TMA-staged configurations for 3 x 3 filters (conv_tma_k3.cu), named
-// F<output channels per CTA>, W<pixels per thread>, <tile rows>; "pc": FMAs
-// paired along input channels.
+// F<output channels per CTA>, W<pixels per thread>, <tile rows>, "r2": two
+// tile rows per consumer warp; "pc": FMAs paired along input channels.
 cudaError_t k3_tma_f4_w5_h4_pc(const ConvArgs &a, cudaStream_t st);
 cudaError_t k3_tma_f4_w5_h4(const ConvArgs &a, cudaStream_t st);
 cudaError_t k3_tma_f4_w5_h8_pc(const ConvArgs &a, cudaStream_t st);
 cudaError_t k3_tma_f4_w3_h4_pc(const ConvArgs &a, cudaStream_t st);
+cudaError_t k3_tma_f4_w5_h8r2(const ConvArgs &a, cudaStream_t st);
 cudaError_t k3_tma_f8_w5_h4(const ConvArgs &a, cudaStream_t st);
 cudaError_t k3_tma_f16_w5_h4(const ConvArgs &a, cudaStream_t st);
 cudaError_t k3_tma_f32_w7_h8(const ConvArgs &a, cudaStream_t st);

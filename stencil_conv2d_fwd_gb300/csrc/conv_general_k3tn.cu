@@ -35,6 +35,7 @@ static const TuneCand k3_n4[] = {
     {"TMA F4 W5 4x160", k3_tma_f4_w5_h4},
     {"TMA F4 W5 8x160 pc", k3_tma_f4_w5_h8_pc},
     {"TMA F4 W3 4x96 pc", k3_tma_f4_w3_h4_pc},
+    {"TMA F4 W5 8x160 r2", k3_tma_f4_w5_h8r2},
 };
 
 const TuneCand *k3_narrow_table(const ConvArgs &a, int *n)

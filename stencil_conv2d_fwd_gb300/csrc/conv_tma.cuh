@@ -34,6 +34,10 @@
 //    input channels of one output channel's tap, the filter bank staged as
 //    [ci / 4][r][s][F_TB][4]).  Otherwise pairs of output channels, as in
 //    conv_general.cuh.
+//  * Rows per consumer warp (H_T): a warp may compute H_T tile rows; the
+//    input rows it reads sit in a register ring (row q in slot q mod H_T),
+//    so each filter unit is loaded once for H_T rows and each input row
+//    once for up to H_T output rows.
 //  * Every wait is bounded: on expiry the kernel records
 //    SC_ERR_DEVICE_TIMEOUT in the status word, the producer lets its copies
 //    still in flight land, and the CTA returns.
@@ -47,12 +51,13 @@
 
 namespace sc {
 
-template <int K_, int F_TB_, int W_T_, int TH_, int C_SH_, int NSTAGE_, int MINB_, bool PAIRC_>
+template <int K_, int F_TB_, int W_T_, int TH_, int H_T_, int C_SH_, int NSTAGE_, int MINB_, bool PAIRC_>
 struct TmaCfg {
     static constexpr int K = K_;
     static constexpr int F_TB = F_TB_;
     static constexpr int W_T = W_T_;
-    static constexpr int TH = TH_;                      // tile rows = consumer warps
+    static constexpr int TH = TH_;                      // tile rows
+    static constexpr int H_T = H_T_;                    // tile rows per consumer warp
     static constexpr int C_SH = C_SH_;                  // channels per step
     static constexpr int NSTAGE = NSTAGE_;
     static constexpr int MINB = MINB_;
@@ -72,9 +77,10 @@ struct TmaCfg {
     static constexpr int STAGE_BYTES = (BOX_BYTES + 1023) & ~1023;
     static constexpr int KK = K * K;
     static constexpr int WIN = W_T + K - 1;
-    static constexpr int NC = TH;                        // consumer warps
+    static constexpr int NC = TH / H_T;                  // consumer warps
     static constexpr int NT = (NC + 1) * 32;             // + the producer warp
     static_assert(W_T % 2 == 1, "W_T must be odd (bank-conflict-free pixel loads)");
+    static_assert(TH % H_T == 0, "whole rows per consumer warp");
     static_assert(C_SH == 8 || C_SH == 16 || C_SH == 32, "C_SH must be 8, 16 or 32");
     static_assert(F_TB % F_T == 0 && 32 % T_X == 0, "bad channel split");
     static_assert(TWB <= 256 && THh <= 256, "TMA box dimensions are at most 256");
@@ -196,17 +202,17 @@ __global__ void __launch_bounds__(C::NT, C::MINB)
         return;
     }
 
-    // ---------------- consumers: warp `warp` computes tile row `warp` -----
+    // ---------------- consumers: warp `warp` computes tile rows warp * H_T .. + H_T - 1
     const int tx = lane % C::T_X;   // output-channel lane
     const int pl = lane / C::T_X;   // pixel lane
     const int cx0 = pl * C::W_T;    // first tile column of this lane
-    // byte offset in a stage of (tile row warp, pixel cx0 + j, chunk cb)
+    // byte offset in a stage of (tile row warp * H_T, pixel cx0 + j, chunk cb)
     uint32_t poff[C::WIN][C::CB];
 #pragma unroll
     for (int j = 0; j < C::WIN; ++j)
 #pragma unroll
         for (int cb = 0; cb < C::CB; ++cb)
-            poff[j][cb] = warp * C::PITCH + (cx0 + j) * C::PXB + ((cb ^ C::key(cx0 + j)) << 4);
+            poff[j][cb] = warp * C::H_T * C::PITCH + (cx0 + j) * C::PXB + ((cb ^ C::key(cx0 + j)) << 4);
 
     float bv[C::F_T];
 #pragma unroll
@@ -219,20 +225,26 @@ __global__ void __launch_bounds__(C::NT, C::MINB)
     const unsigned char *wbase = reinterpret_cast<const unsigned char *>(w_res);
     auto ld4 = [](const unsigned char *p) { return *reinterpret_cast<const float4 *>(p); };
 
-    constexpr int AF = C::PAIRC ? 1 : C::F_T, AW = C::PAIRC ? 1 : C::W_T;
-    constexpr int PF = C::PAIRC ? C::F_T : 1, PW = C::PAIRC ? C::W_T : 1;
+    // accumulators [output row][channel][pixel]: channel pairing uses acc,
+    // PAIRC the (even, odd input channel) partial sums acc2
+    constexpr int AH = C::PAIRC ? 1 : C::H_T, AF = C::PAIRC ? 1 : C::F_T, AW = C::PAIRC ? 1 : C::W_T;
+    constexpr int PH = C::PAIRC ? C::H_T : 1, PF = C::PAIRC ? C::F_T : 1, PW = C::PAIRC ? C::W_T : 1;
     int it = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-        float acc[AF][AW];
-        float2 acc2[PF][PW];
+        float acc[AH][AF][AW];
+        float2 acc2[PH][PF][PW];
 #pragma unroll
-        for (int f = 0; f < AF; ++f)
+        for (int h = 0; h < AH; ++h)
 #pragma unroll
-            for (int j = 0; j < AW; ++j) acc[f][j] = 0.0f;
+            for (int f = 0; f < AF; ++f)
 #pragma unroll
-        for (int f = 0; f < PF; ++f)
+                for (int j = 0; j < AW; ++j) acc[h][f][j] = 0.0f;
 #pragma unroll
-            for (int j = 0; j < PW; ++j) acc2[f][j] = make_float2(0.0f, 0.0f);
+        for (int h = 0; h < PH; ++h)
+#pragma unroll
+            for (int f = 0; f < PF; ++f)
+#pragma unroll
+                for (int j = 0; j < PW; ++j) acc2[h][f][j] = make_float2(0.0f, 0.0f);
 
         for (int k = 0; k < nk; ++k, ++it) {
             const int slot = it % C::NSTAGE;
@@ -250,11 +262,18 @@ __global__ void __launch_bounds__(C::NT, C::MINB)
             const unsigned char *wk = wbase + (size_t)k * (C::CB * C::KK * C::F_TB * 16);
 #pragma unroll
             for (int cb = 0; cb < C::CB; ++cb) {
+                // register ring of input rows: row q (from the warp's first
+                // tile row) in pw[q % H_T]; output row h uses rows h .. h + K - 1
+                float4 pw[C::H_T][C::WIN];
+#pragma unroll
+                for (int q = 0; q < C::H_T - 1; ++q)
+#pragma unroll
+                    for (int j = 0; j < C::WIN; ++j) pw[q % C::H_T][j] = ld4(pa[j][cb] + q * C::PITCH);
 #pragma unroll
                 for (int r = 0; r < C::K; ++r) {
-                    float4 px[C::WIN];
+                    const int qn = r + C::H_T - 1;   // the row this filter row brings in
 #pragma unroll
-                    for (int j = 0; j < C::WIN; ++j) px[j] = ld4(pa[j][cb] + r * C::PITCH);
+                    for (int j = 0; j < C::WIN; ++j) pw[qn % C::H_T][j] = ld4(pa[j][cb] + qn * C::PITCH);
                     if constexpr (C::PAIRC) {
 #pragma unroll
                         for (int s = 0; s < C::K; ++s) {
@@ -266,17 +285,21 @@ __global__ void __launch_bounds__(C::NT, C::MINB)
 #pragma unroll
                                 for (int e = 0; e < 4; ++e) wv[4 * g + e] = ld4(wu + (g * (C::F_TB / C::NG) + e) * 16);
 #pragma unroll
-                            for (int j = 0; j < C::W_T; ++j)
+                            for (int h = 0; h < C::H_T; ++h) {
+                                const float4(&px)[C::WIN] = pw[(r + h) % C::H_T];
 #pragma unroll
-                                for (int f = 0; f < C::F_T; ++f)
-                                    acc2[f][j] = __ffma2_rn(make_float2(wv[f].x, wv[f].y),
-                                                            make_float2(px[j + s].x, px[j + s].y), acc2[f][j]);
+                                for (int j = 0; j < C::W_T; ++j)
 #pragma unroll
-                            for (int j = 0; j < C::W_T; ++j)
+                                    for (int f = 0; f < C::F_T; ++f)
+                                        acc2[h][f][j] = __ffma2_rn(make_float2(wv[f].x, wv[f].y),
+                                                                   make_float2(px[j + s].x, px[j + s].y), acc2[h][f][j]);
 #pragma unroll
-                                for (int f = 0; f < C::F_T; ++f)
-                                    acc2[f][j] = __ffma2_rn(make_float2(wv[f].z, wv[f].w),
-                                                            make_float2(px[j + s].z, px[j + s].w), acc2[f][j]);
+                                for (int j = 0; j < C::W_T; ++j)
+#pragma unroll
+                                    for (int f = 0; f < C::F_T; ++f)
+                                        acc2[h][f][j] = __ffma2_rn(make_float2(wv[f].z, wv[f].w),
+                                                                   make_float2(px[j + s].z, px[j + s].w), acc2[h][f][j]);
+                            }
                         }
                     } else {
 #pragma unroll
@@ -295,16 +318,20 @@ __global__ void __launch_bounds__(C::NT, C::MINB)
                                     wv[4 * g + 3] = q.w;
                                 }
 #pragma unroll
-                                for (int j = 0; j < C::W_T; ++j) {
-                                    const float4 p = px[j + s];
-                                    const float v = c == 0 ? p.x : (c == 1 ? p.y : (c == 2 ? p.z : p.w));
-                                    const float2 vv = make_float2(v, v);
+                                for (int h = 0; h < C::H_T; ++h) {
+                                    const float4(&px)[C::WIN] = pw[(r + h) % C::H_T];
 #pragma unroll
-                                    for (int f = 0; f < C::F_T; f += 2) {
-                                        float2 a2 = make_float2(acc[f][j], acc[f + 1][j]);
-                                        a2 = __ffma2_rn(make_float2(wv[f], wv[f + 1]), vv, a2);
-                                        acc[f][j] = a2.x;
-                                        acc[f + 1][j] = a2.y;
+                                    for (int j = 0; j < C::W_T; ++j) {
+                                        const float4 p = px[j + s];
+                                        const float v = c == 0 ? p.x : (c == 1 ? p.y : (c == 2 ? p.z : p.w));
+                                        const float2 vv = make_float2(v, v);
+#pragma unroll
+                                        for (int f = 0; f < C::F_T; f += 2) {
+                                            float2 a2 = make_float2(acc[h][f][j], acc[h][f + 1][j]);
+                                            a2 = __ffma2_rn(make_float2(wv[f], wv[f + 1]), vv, a2);
+                                            acc[h][f][j] = a2.x;
+                                            acc[h][f + 1][j] = a2.y;
+                                        }
                                     }
                                 }
                             }
@@ -318,28 +345,31 @@ __global__ void __launch_bounds__(C::NT, C::MINB)
         }
 
         // epilogue: bias, activation, 16-byte NHWC stores of 4 output channels
-        auto res = [&](int f, int j) {
-            if constexpr (C::PAIRC) return acc2[f][j].x + acc2[f][j].y;
-            else return acc[f][j];
+        auto res = [&](int h, int f, int j) {
+            if constexpr (C::PAIRC) return acc2[h][f][j].x + acc2[h][f][j].y;
+            else return acc[h][f][j];
         };
         int n, y0, x0;
         decode(t, n, y0, x0);
-        const int gy = y0 + warp;
-        if (gy < H) {
 #pragma unroll
-            for (int g = 0; g < C::NG; ++g) {
-                const int co = co0 + g * (C::F_TB / C::NG) + 4 * tx;
-                if (co < Cout) {
+        for (int h = 0; h < C::H_T; ++h) {
+            const int gy = y0 + warp * C::H_T + h;
+            if (gy < H) {
 #pragma unroll
-                    for (int j = 0; j < C::W_T; ++j) {
-                        const int gx = x0 + cx0 + j;
-                        if (gx < W) {
-                            float4 o;
-                            o.x = relu_if(res(4 * g + 0, j) + bv[4 * g + 0], act);
-                            o.y = relu_if(res(4 * g + 1, j) + bv[4 * g + 1], act);
-                            o.z = relu_if(res(4 * g + 2, j) + bv[4 * g + 2], act);
-                            o.w = relu_if(res(4 * g + 3, j) + bv[4 * g + 3], act);
-                            *reinterpret_cast<float4 *>(y + ((((long long)n * H + gy) * W + gx) * Cout + co)) = o;
+                for (int g = 0; g < C::NG; ++g) {
+                    const int co = co0 + g * (C::F_TB / C::NG) + 4 * tx;
+                    if (co < Cout) {
+#pragma unroll
+                        for (int j = 0; j < C::W_T; ++j) {
+                            const int gx = x0 + cx0 + j;
+                            if (gx < W) {
+                                float4 o;
+                                o.x = relu_if(res(h, 4 * g + 0, j) + bv[4 * g + 0], act);
+                                o.y = relu_if(res(h, 4 * g + 1, j) + bv[4 * g + 1], act);
+                                o.z = relu_if(res(h, 4 * g + 2, j) + bv[4 * g + 2], act);
+                                o.w = relu_if(res(h, 4 * g + 3, j) + bv[4 * g + 3], act);
+                                *reinterpret_cast<float4 *>(y + ((((long long)n * H + gy) * W + gx) * Cout + co)) = o;
+                            }
                         }
                     }
                 }

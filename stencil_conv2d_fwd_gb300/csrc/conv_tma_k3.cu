@@ -23,42 +23,46 @@ PFN_cuTensorMapEncodeTiled_v12000 conv_tma_encoder()
     return fn;
 }
 
-// <K, F_TB, W_T, TH, C_SH, NSTAGE, MINB, PAIRC>
+// <K, F_TB, W_T, TH, H_T, C_SH, NSTAGE, MINB, PAIRC>
 cudaError_t k3_tma_f4_w5_h4_pc(const ConvArgs &a, cudaStream_t st)
 {
-    return launch_conv_tma<TmaCfg<3, 4, 5, 4, 8, 3, 2, true>>(a, st);
+    return launch_conv_tma<TmaCfg<3, 4, 5, 4, 1, 8, 3, 2, true>>(a, st);
 }
 cudaError_t k3_tma_f4_w5_h4(const ConvArgs &a, cudaStream_t st)
 {
-    return launch_conv_tma<TmaCfg<3, 4, 5, 4, 8, 3, 2, false>>(a, st);
+    return launch_conv_tma<TmaCfg<3, 4, 5, 4, 1, 8, 3, 2, false>>(a, st);
 }
 cudaError_t k3_tma_f4_w5_h8_pc(const ConvArgs &a, cudaStream_t st)
 {
-    return launch_conv_tma<TmaCfg<3, 4, 5, 8, 8, 3, 1, true>>(a, st);
+    return launch_conv_tma<TmaCfg<3, 4, 5, 8, 1, 8, 3, 1, true>>(a, st);
 }
 cudaError_t k3_tma_f4_w3_h4_pc(const ConvArgs &a, cudaStream_t st)
 {
-    return launch_conv_tma<TmaCfg<3, 4, 3, 4, 8, 3, 3, true>>(a, st);
+    return launch_conv_tma<TmaCfg<3, 4, 3, 4, 1, 8, 3, 3, true>>(a, st);
+}
+cudaError_t k3_tma_f4_w5_h8r2(const ConvArgs &a, cudaStream_t st)
+{
+    return launch_conv_tma<TmaCfg<3, 4, 5, 8, 2, 8, 2, 2, false>>(a, st);
 }
 cudaError_t k3_tma_f8_w5_h4(const ConvArgs &a, cudaStream_t st)
 {
-    return launch_conv_tma<TmaCfg<3, 8, 5, 4, 8, 3, 2, false>>(a, st);
+    return launch_conv_tma<TmaCfg<3, 8, 5, 4, 1, 8, 3, 2, false>>(a, st);
 }
 cudaError_t k3_tma_f16_w5_h4(const ConvArgs &a, cudaStream_t st)
 {
-    return launch_conv_tma<TmaCfg<3, 16, 5, 4, 8, 3, 2, false>>(a, st);
+    return launch_conv_tma<TmaCfg<3, 16, 5, 4, 1, 8, 3, 2, false>>(a, st);
 }
 cudaError_t k3_tma_f32_w7_h8(const ConvArgs &a, cudaStream_t st)
 {
-    return launch_conv_tma<TmaCfg<3, 32, 7, 8, 8, 3, 1, false>>(a, st);
+    return launch_conv_tma<TmaCfg<3, 32, 7, 8, 1, 8, 3, 1, false>>(a, st);
 }
 cudaError_t k3_tma_f32_w5_h8(const ConvArgs &a, cudaStream_t st)
 {
-    return launch_conv_tma<TmaCfg<3, 32, 5, 8, 8, 3, 1, false>>(a, st);
+    return launch_conv_tma<TmaCfg<3, 32, 5, 8, 1, 8, 3, 1, false>>(a, st);
 }
 cudaError_t k3_tma_f64_w7_h8(const ConvArgs &a, cudaStream_t st)
 {
-    return launch_conv_tma<TmaCfg<3, 64, 7, 8, 8, 3, 1, false>>(a, st);
+    return launch_conv_tma<TmaCfg<3, 64, 7, 8, 1, 8, 3, 1, false>>(a, st);
 }
 
 // Default for more than 16 output channels: 64 per CTA above 32, else 32
