@@ -248,6 +248,23 @@ int sc_test_conv_candidate(const float *x, const float *w, const float *b, float
                            int act, int candidate, sc_stream_t stream);
 
 /*
+ * sc_test_conv_wait_expiry: test hook for the device-status path, not part
+ * of the operation.  Runs conv2d_fwd's TMA-staged kernel (NHWC, 3 x 3, no
+ * activation, the default tile configuration for Cout) with copy
+ * `drop_copy` (0-based, in each CTA's issue order) never issued, so the
+ * time-bounded waits for it expire after `timeout_us` microseconds (a
+ * CTA's consumers on the stage, then its producer on the stage's release).
+ * The kernel then records SC_ERR_DEVICE_TIMEOUT (read and cleared by
+ * sc_last_device_status), lets its other copies land and returns; the
+ * context stays usable.  `y` is left partly written.  Cin % 4 == 0,
+ * Cout % 4 == 0, 16-byte aligned x and y; SC_ERR_UNSUPPORTED where the
+ * TMA kernel does not apply (a filter bank above its shared-memory limit).
+ */
+int sc_test_conv_wait_expiry(const float *x, const float *w, const float *b, float *y,
+                             int N, int H, int W, int Cin, int Cout, int drop_copy, int timeout_us,
+                             sc_stream_t stream);
+
+/*
  * sc_test_stencil_wait_expiry: test hook for the device-status path, not
  * part of the operation.  Runs stencil_pipeline_fwd's TMA kernel with the
  * copy of row chunk `drop_copy` (0-based, per warp) never issued, so each

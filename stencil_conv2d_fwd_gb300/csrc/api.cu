@@ -397,4 +397,25 @@ int sc_test_stencil_wait_expiry(const float *in, float *out, int H, int W, int d
     return e == cudaSuccess ? SC_OK : cuda_fail(e);
 }
 
+int sc_test_conv_wait_expiry(const float *x, const float *w, const float *b, float *y, int N, int H, int W, int Cin,
+                             int Cout, int drop_copy, int timeout_us, sc_stream_t stream)
+{
+    if (!x || !w || !y) return SC_ERR_NULL;
+    const long long nx = checked_count({N, H, W, Cin});
+    const long long ny = checked_count({N, H, W, Cout});
+    const long long nw = checked_count({Cout, Cin, 3, 3});
+    if (nx < 0 || ny < 0 || nw < 0 || drop_copy < 0 || timeout_us < 1) return SC_ERR_SHAPE;
+    if ((Cin % 4) != 0 || (Cout % 4) != 0) return SC_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(y)) return SC_ERR_ALIGN;
+    const size_t ybytes = (size_t)ny * sizeof(float);
+    if (overlaps(y, ybytes, x, (size_t)nx * sizeof(float)) || overlaps(y, ybytes, w, (size_t)nw * sizeof(float)) ||
+        overlaps(y, ybytes, b, b ? (size_t)Cout * sizeof(float) : 0))
+        return SC_ERR_ALIAS;
+    sc::ConvArgs a{x, w, b, y, N, H, W, Cin, Cout, 3, 3, SC_ACT_NONE};
+    const cudaError_t e = sc::launch_conv_tma_k3_test(a, drop_copy, 1000ull * (unsigned long long)timeout_us,
+                                                      reinterpret_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return SC_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? SC_OK : cuda_fail(e);
+}
+
 }  // extern "C"

@@ -132,7 +132,8 @@ template <class C>
 __global__ void __launch_bounds__(C::NT, C::MINB)
     conv_tma_kernel(const __grid_constant__ CUtensorMap tm, const float *__restrict__ w,
                     const float *__restrict__ bias, float *__restrict__ y, int N, int H, int W, int Cin, int Cout,
-                    int R, int S, int act, int tiles_x, int tiles_y, int *status, unsigned long long timeout_ns)
+                    int R, int S, int act, int tiles_x, int tiles_y, int *status, unsigned long long timeout_ns,
+                    int drop_copy)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // the dynamic buffer is 1024-byte aligned in practice; align explicitly
@@ -190,8 +191,9 @@ __global__ void __launch_bounds__(C::NT, C::MINB)
                 // the consumers' reads of this stage come before the copy's writes
                 fence_proxy_async_smem();
                 mbar_arrive_expect_tx(full(slot), C::BOX_BYTES);
-                tma_load_4d(stage0 + slot * C::STAGE_BYTES, &tm, k * C::C_SH, x0 - C::K / 2, y0 - C::K / 2, n,
-                            full(slot));
+                if (issued != drop_copy)   // test hook: that copy is never issued
+                    tma_load_4d(stage0 + slot * C::STAGE_BYTES, &tm, k * C::C_SH, x0 - C::K / 2, y0 - C::K / 2, n,
+                                full(slot));
             }
         }
         if (failed) atomicExch(status, kDeviceTimeout);
@@ -387,8 +389,12 @@ constexpr size_t kTmaFilterBytes = 160 * 1024;
 // Opt-in shared memory per CTA on sm_103.
 constexpr size_t kTmaMaxSmem = 227 * 1024;
 
+// drop_copy >= 0 leaves that copy of every CTA (0-based, in issue order)
+// un-issued, so the waits for it expire after timeout_ns (tests of the
+// device-status path).
 template <class C>
-cudaError_t launch_conv_tma(const ConvArgs &a, cudaStream_t st)
+cudaError_t launch_conv_tma(const ConvArgs &a, cudaStream_t st, int drop_copy = -1,
+                            unsigned long long timeout_ns = 1000000000ull)
 {
     const int cin_pad = (a.Cin + C::C_SH - 1) / C::C_SH * C::C_SH;
     if ((size_t)cin_pad * C::KK * C::F_TB * 4 > kTmaFilterBytes || a.R > C::K || a.S > C::K || (a.Cin & 3))
@@ -443,8 +449,8 @@ cudaError_t launch_conv_tma(const ConvArgs &a, cudaStream_t st)
     if (gx > nt) gx = nt;
     if (gx < 1) gx = 1;
     conv_tma_kernel<C><<<dim3((unsigned)gx, groups), C::NT, smem, st>>>(
-        tm, a.w, a.b, a.y, a.N, a.H, a.W, a.Cin, a.Cout, a.R, a.S, a.act, tiles_x, tiles_y, status,
-        1000000000ull);
+        tm, a.w, a.b, a.y, a.N, a.H, a.W, a.Cin, a.Cout, a.R, a.S, a.act, tiles_x, tiles_y, status, timeout_ns,
+        drop_copy);
     return cudaGetLastError();
 }
 

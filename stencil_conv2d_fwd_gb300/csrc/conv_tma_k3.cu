@@ -74,6 +74,18 @@ cudaError_t launch_conv_tma_k3_wide(const ConvArgs &a, cudaStream_t st)
     return waste56 < waste40 ? k3_tma_f32_w7_h8(a, st) : k3_tma_f32_w5_h8(a, st);
 }
 
+// The default configuration of the shape's class with one copy per CTA left
+// un-issued and waits bounded by timeout_ns (sc_test_conv_wait_expiry).
+cudaError_t launch_conv_tma_k3_test(const ConvArgs &a, int drop_copy, unsigned long long timeout_ns,
+                                    cudaStream_t st)
+{
+    if (a.Cout <= 4) return launch_conv_tma<TmaCfg<3, 4, 5, 4, 1, 8, 3, 2, false>>(a, st, drop_copy, timeout_ns);
+    if (a.Cout <= 8) return launch_conv_tma<TmaCfg<3, 8, 5, 4, 1, 8, 3, 2, false>>(a, st, drop_copy, timeout_ns);
+    if (a.Cout <= 16) return launch_conv_tma<TmaCfg<3, 16, 5, 4, 1, 8, 3, 2, false>>(a, st, drop_copy, timeout_ns);
+    if (a.Cout <= 32) return launch_conv_tma<TmaCfg<3, 32, 5, 8, 1, 8, 3, 1, false>>(a, st, drop_copy, timeout_ns);
+    return launch_conv_tma<TmaCfg<3, 64, 7, 8, 1, 8, 3, 1, false>>(a, st, drop_copy, timeout_ns);
+}
+
 // Default for 16 or fewer output channels: the TMA-staged kernel, one
 // output-channel group per CTA; cudaErrorNotSupported where it does not
 // apply (the caller then uses conv_general_k3n.cu's configurations).

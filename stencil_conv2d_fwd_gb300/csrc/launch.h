@@ -26,6 +26,10 @@ cudaError_t launch_conv_general_k7(const ConvArgs &a, cudaStream_t st);
 // where it does not apply.
 cudaError_t launch_conv_tma_k3_narrow(const ConvArgs &a, cudaStream_t st);
 cudaError_t launch_conv_tma_k3_wide(const ConvArgs &a, cudaStream_t st);
+// Test hook (sc_test_conv_wait_expiry): the default configuration with
+// copy `drop_copy` of every CTA never issued and waits bounded by timeout_ns.
+cudaError_t launch_conv_tma_k3_test(const ConvArgs &a, int drop_copy, unsigned long long timeout_ns,
+                                    cudaStream_t st);
 
 // NHWC convolution: picks the single-input-channel kernel or the general
 // kernel for K = max(R, S) (api.cu).

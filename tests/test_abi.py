@@ -95,3 +95,13 @@ def test_pipeline_and_repack_argument_errors():
     assert sc.sc_repack(A16, A16 + 16, 1, 4, 2, 2, 0, 1, stream=0) == sc.SC_ERR_ALIAS
     assert sc.sc_measure_ffma_peak(None, 1, 1, stream=0) == sc.SC_ERR_NULL
     assert sc.sc_measure_ffma_peak(A16, 0, 1, stream=0) == sc.SC_ERR_SHAPE
+
+
+def test_conv_wait_expiry_hook_argument_errors():
+    # host-side checks only: nothing is launched
+    assert sc.sc_test_conv_wait_expiry(None, A16, None, B16, 1, 4, 4, 4, 4, 0, 10, stream=0) == sc.SC_ERR_NULL
+    assert sc.sc_test_conv_wait_expiry(A16, A16, None, B16, 1, 4, 4, 4, 4, -1, 10, stream=0) == sc.SC_ERR_SHAPE
+    assert sc.sc_test_conv_wait_expiry(A16, A16, None, B16, 1, 4, 4, 4, 4, 0, 0, stream=0) == sc.SC_ERR_SHAPE
+    assert sc.sc_test_conv_wait_expiry(A16, A16, None, B16, 1, 4, 4, 6, 4, 0, 10, stream=0) == sc.SC_ERR_UNSUPPORTED
+    assert sc.sc_test_conv_wait_expiry(A16 + 4, A16, None, B16, 1, 4, 4, 4, 4, 0, 10, stream=0) == sc.SC_ERR_ALIGN
+    assert sc.sc_test_conv_wait_expiry(A16, A16, None, A16, 1, 4, 4, 4, 4, 0, 10, stream=0) == sc.SC_ERR_ALIAS

@@ -154,3 +154,26 @@ def test_misaligned_pointer_rejected_without_launch(cuda_dev, sc):
     assert rc == sc.SC_ERR_ALIGN
     torch.cuda.synchronize()
     assert (y == 3.0).all()
+
+
+@pytest.mark.parametrize("Cout", [4, 32])
+def test_tma_kernel_bounded_wait_expiry(oracle_mod, cuda_dev, sc, Cout):
+    """Failure detection without a fault: copy 1 of every CTA of the
+    TMA-staged convolution is never issued; the waits for it expire (2 ms),
+    the kernel records SC_ERR_DEVICE_TIMEOUT and returns; the next call on
+    the same context is correct."""
+    from parity_util import nchw_to_nhwc
+    N, Cin, H, W = 1, 32, 24, 200
+    c = S.conv_case(990 + Cout, N, Cin, Cout, H, W, 3, 3, act=0)
+    L = c.layers[0]
+    xd = torch.from_numpy(nchw_to_nhwc(c.x)).to(cuda_dev)
+    wd = torch.from_numpy(np.ascontiguousarray(L.w)).to(cuda_dev)
+    bd = torch.from_numpy(L.b).to(cuda_dev)
+    yd = torch.empty(N * H * W * Cout, device=cuda_dev)
+    assert sc.sc_last_device_status() == sc.SC_OK
+    rc = sc.sc_test_conv_wait_expiry(xd, wd, bd, yd, N, H, W, Cin, Cout, 1, 2000)
+    assert rc == sc.SC_OK, sc.sc_status_string(rc)
+    assert sc.sc_last_device_status() == sc.SC_ERR_DEVICE_TIMEOUT
+    assert sc.sc_last_device_status() == sc.SC_OK          # read clears it
+    y, yr, a = _one(oracle_mod, cuda_dev, c.x, L)           # context still usable
+    assert_conv_close(y, yr, a, what=f"after the expiry test, Cout={Cout}")
