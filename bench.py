@@ -349,6 +349,8 @@ def run_ours(args, rank, world, local):
     # ---- oracle on the host cores (rank 0 only)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl, min_seconds=10.0)
+        if not args.no_per_config:
+            result["cpu_baseline"]["per_config"] = oracle_per_config(S)
 
     if world > 1:
         torch.distributed.barrier()
@@ -632,6 +634,61 @@ def cpu_baseline(wl, min_seconds=10.0, rows=None):
     return {"value": round(px * flops_px / dt / 1e9, 3), "unit": "GFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{passes} pass(es) of the 3-layer net over {rows} of 720 rows x 1280 (fp64 C oracle, "
                       f"OpenMP), {dt:.1f} s"}
+
+
+def oracle_per_config(S, min_seconds=0.5):
+    """The oracle on every workload, on the machine's host cores: all OpenMP
+    threads for every workload and one thread for workloads 1, 2 and 5, each
+    on a bounded sample (whole images for 1 and 2, one image of the batch
+    for 4, a row strip for 3 and 5), repeated for at least min_seconds.
+    Output Mpixel/s (and GFLOP/s for the convolutions)."""
+    import oracle
+    cores = oracle.set_threads(0)
+
+    def timed(fn):
+        n, t0 = 0, time.perf_counter()
+        while True:
+            px = fn()
+            n += 1
+            dt = time.perf_counter() - t0
+            if dt >= min_seconds:
+                return n * px / dt, n, dt
+
+    def conv_sample(wl, images=None):
+        x = wl.x if images is None else wl.x[:images]
+        L = wl.layers[0]
+
+        def fn():
+            oracle.conv2d_nchw(x, L.w, L.b, L.act, with_scale=False)
+            return x.shape[0] * wl.h * wl.w
+        return fn, 2 * L.cin * L.cout * L.r * L.s
+
+    w3 = S.config(3)
+    w5 = S.config(5)
+    strip5 = 64
+    cases = {
+        "1": (*conv_sample(S.config(1)), "the 64x64 image", True),
+        "2": (*conv_sample(S.config(2)), "the 128x128 image", True),
+        "3": (lambda: oracle_net_pass(oracle, w3, 16), sum(2 * L.cin * L.cout * L.r * L.s for L in w3.layers),
+              "a 16-row strip of the 3-layer net", False),
+        "4": (*conv_sample(S.config(4), images=1), "one 56x56 image of the 32", False),
+        "5": (lambda: (oracle.stencil_pipeline(w5.img, rows=(0, strip5)), strip5 * w5.w)[1], None,
+              f"a {strip5}-row strip of the 4096x4096 image", True),
+    }
+    out = {}
+    for name, (fn, flops_px, sample, single) in cases.items():
+        runs = [(cores, "openmp")] + ([(1, "1 thread")] if single else [])
+        ent = {"sample": sample}
+        for threads, tag in runs:
+            oracle.set_threads(threads)
+            px_s, n, dt = timed(fn)
+            r = {"mpixel_per_s": round(px_s / 1e6, 4), "threads": threads, "calls": n, "seconds": round(dt, 2)}
+            if flops_px:
+                r["gflops"] = round(px_s * flops_px / 1e9, 3)
+            ent[tag] = r
+        oracle.set_threads(cores)
+        out[name] = ent
+    return out
 
 
 def run_reference(args, rank, world):

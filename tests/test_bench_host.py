@@ -27,3 +27,14 @@ def test_oracle_strip_pass_counts_pixels():
 
 def test_profiled_traffic_absent_or_stale_is_none():
     assert bench.profiled_traffic("no-such-kernel", "0" * 16) is None
+
+
+def test_oracle_per_config_covers_every_workload():
+    # every workload timed with all threads; 1, 2 and 5 also single-threaded
+    r = bench.oracle_per_config(S, min_seconds=0.01)
+    assert sorted(r) == ["1", "2", "3", "4", "5"]
+    for name, ent in r.items():
+        assert ent["openmp"]["mpixel_per_s"] > 0 and ent["openmp"]["calls"] >= 1
+        assert ("1 thread" in ent) == (name in ("1", "2", "5"))
+        if name != "5":
+            assert ent["openmp"]["gflops"] > 0
