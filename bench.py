@@ -69,6 +69,25 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value, world, device=None):
+    """The largest of the ranks' values (the job's step time is its slowest
+    rank's); `device` holds the reduction tensor (the GPU for NCCL, None =
+    CPU for gloo)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, units_per_rank, ms):
+    """Whole-job throughput: every rank processes units_per_rank per step of
+    ms milliseconds (weak scaling, replicas)."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -265,13 +284,9 @@ def run_ours(args, rank, world, local):
 
     layer_ms = [[ev[k][li][0].elapsed_time(ev[k][li][1]) for k in range(K)] for li in range(len(layers))]
     step_ms = [ev[k][0][0].elapsed_time(ev[k][-1][1]) for k in range(K)]
-    ms_step = sum(step_ms) / K
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
-    value = world * flops_step / (ms_step * 1e-3) / 1e9
-    mpix = world * N * H * W / (ms_step * 1e-3) / 1e6
+    ms_step = max_over_ranks(sum(step_ms) / K, world, dev)
+    value = job_rate(world, flops_step, ms_step) / 1e9
+    mpix = job_rate(world, N * H * W, ms_step) / 1e6
 
     # dominant kernel: the layer with the largest mean time
     means = [sum(v) / K for v in layer_ms]
@@ -334,8 +349,8 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
         if k >= args.warmup:
             e2e_ms.append(e0.elapsed_time(e1))
-    e2e_step = sum(e2e_ms) / K
-    result["e2e"] = {"value": round(world * flops_step / (e2e_step * 1e-3) / 1e9, 2), "unit": "GFLOP/s",
+    e2e_step = max_over_ranks(sum(e2e_ms) / K, world, dev)
+    result["e2e"] = {"value": round(job_rate(world, flops_step, e2e_step) / 1e9, 2), "unit": "GFLOP/s",
                      "ms_per_step": round(e2e_step, 4),
                      "h2d_bytes_per_step": x_host.numel() * 4, "d2h_bytes_per_step": y_host.numel() * 4}
 
