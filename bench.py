@@ -358,8 +358,9 @@ def run_ours(args, rank, world, local):
     if not args.no_per_config:
         result["per_config"] = per_config(sc, S, dev, stream, flush, fp32_peak_tflops, hbm_gbs, hbm_src)
 
-    # ---- measured FP32 FMA rate (context for the nominal peak)
+    # ---- measured FP32 FMA rate and HBM copy bandwidth (context for the peaks)
     result["ffma_probe_tflops"] = ffma_probe(sc, dev, stream, n_sm)
+    result["hbm_probe_gbs"] = hbm_probe(dev, stream)
 
     # ---- oracle on the host cores (rank 0 only)
     if rank == 0 and not args.no_cpu_baseline:
@@ -597,6 +598,26 @@ def per_config(sc, S, dev, stream, flush, fp32_tflops, hbm_gbs, hbm_src):
     out["_peaks"] = {"fp32_tflops": round(fp32_tflops, 2), "hbm_gbs": hbm_gbs, "hbm_source": hbm_src,
                      "fp32_source": "nominal: SMs x 128 FP32 lanes x 2 x max SM clock"}
     return out
+
+
+def hbm_probe(dev, stream, nbytes=1 << 30, reps=5):
+    """Device-to-device copy of nbytes (2 x nbytes of HBM traffic per copy;
+    buffers 8x the L2), best of reps: context for the measured HBM peak."""
+    import torch
+    src = torch.ones(nbytes // 4, device=dev)
+    dst = torch.empty_like(src)
+    dst.copy_(src)
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dst.copy_(src)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    del src, dst
+    return round(2 * nbytes / (best * 1e-3) / 1e9, 1)
 
 
 def ffma_probe(sc, dev, stream, n_sm):
