@@ -96,6 +96,9 @@ C1_SHAPES = [
     # W % 4 == 0 (the register-ring kernel): every filter size, bands that are
     # not a multiple of K rows, a 2-pixel-wide strip per lane group
     (1, 32, 17, 96, 7, 7), (1, 8, 9, 44, 1, 1), (2, 16, 13, 52, 3, 3), (1, 4, 7, 8, 3, 5), (1, 1, 23, 36, 5, 5),
+    # more than 16 channels, W % 4 == 0 (two output rows per pass): odd band
+    # ends, channel groups past Cout, 3x3 and 5x5
+    (1, 32, 13, 44, 3, 3), (2, 24, 9, 40, 5, 5), (1, 32, 7, 8, 5, 5), (1, 64, 11, 36, 3, 3),
 ]
 
 
