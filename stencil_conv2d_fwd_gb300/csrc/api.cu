@@ -72,15 +72,23 @@ cudaError_t launch_conv_nhwc(const ConvArgs &a, cudaStream_t st)
 
 int *device_status_ptr()
 {
-    static int *addr[64] = {};
+    static std::atomic<int *> addr[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    if (!addr[dev]) {
+    int *a = addr[dev].load(std::memory_order_acquire);
+    if (!a) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
-        addr[dev] = static_cast<int *>(p);
+        a = static_cast<int *>(p);
+        addr[dev].store(a, std::memory_order_release);
     }
-    return addr[dev];
+    return a;
+}
+
+std::mutex &launch_cache_mutex()
+{
+    static std::mutex m;
+    return m;
 }
 
 // Temporary buffers come from one library-private memory pool per device
@@ -137,14 +145,17 @@ void workspace_trim()
 
 int device_sm_count()
 {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+    if (dev >= 0 && dev < 64) {
+        const int c = cached[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
         n = 148;
-    if (dev >= 0 && dev < 64) cached[dev] = n;
+    if (dev >= 0 && dev < 64) cached[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 

@@ -406,25 +406,14 @@ cudaError_t launch_gen(const ConvArgs &a, cudaStream_t st)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    // per device: the largest dynamic shared memory opted in so far, and the
-    // resident CTAs per SM at the last size queried
-    static int allowed[64] = {0};
-    static int per_sm[64] = {0};
-    static int per_sm_smem[64] = {0};
-    if (smem > 48 * 1024 && allowed[dev] < (int)smem) {
-        e = cudaFuncSetAttribute(conv_general_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        allowed[dev] = (int)smem;
-    }
-    if (per_sm_smem[dev] != (int)smem) {
-        int b = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, conv_general_kernel<C>, C::NT, smem);
-        if (e != cudaSuccess) return e;
-        per_sm[dev] = b > 0 ? b : 1;
-        per_sm_smem[dev] = (int)smem;
-    }
+    static KernelCache cache;
+    e = ensure_dynamic_smem(cache, dev, conv_general_kernel<C>, (int)smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 1;
+    e = resident_ctas(cache, dev, conv_general_kernel<C>, C::NT, (int)smem, &per_sm);
+    if (e != cudaSuccess) return e;
     // persistent grid: the resident CTAs, shared out among the output-channel groups
-    const long long slots = (long long)per_sm[dev] * device_sm_count();
+    const long long slots = (long long)per_sm * device_sm_count();
     long long gx = (slots + groups - 1) / groups;
     if (gx > nt) gx = nt;
     if (gx < 1) gx = 1;

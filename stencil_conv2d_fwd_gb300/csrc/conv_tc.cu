@@ -560,14 +560,10 @@ static cudaError_t launch_tc_cg(const ConvArgs &a, cudaStream_t st)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    static int allowed[64] = {0};
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (allowed[dev] < (int)g.smem_bytes) {
-        e = cudaFuncSetAttribute(conv_tc_kernel<CG, OP, YBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)g.smem_bytes);
-        if (e != cudaSuccess) return e;
-        allowed[dev] = (int)g.smem_bytes;
-    }
+    static KernelCache cache;
+    e = ensure_dynamic_smem(cache, dev, conv_tc_kernel<CG, OP, YBF16>, (int)g.smem_bytes);
+    if (e != cudaSuccess) return e;
     const int per_group = device_sm_count() / groups > 0 ? device_sm_count() / groups : 1;
     const int grid = g.ntiles < per_group ? g.ntiles : per_group;
     conv_tc_kernel<CG, OP, YBF16><<<dim3(grid, groups), tc::NTHREADS, g.smem_bytes, st>>>(

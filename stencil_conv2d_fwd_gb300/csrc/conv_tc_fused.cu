@@ -519,14 +519,10 @@ static cudaError_t launch_fused_cg(const FusedArgs &a, cudaStream_t st)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    static int allowed[64] = {0};
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (allowed[dev] < (int)g.smem_bytes) {
-        e = cudaFuncSetAttribute(conv_tc_fused2_kernel<CG2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)g.smem_bytes);
-        if (e != cudaSuccess) return e;
-        allowed[dev] = (int)g.smem_bytes;
-    }
+    static KernelCache cache;
+    e = ensure_dynamic_smem(cache, dev, conv_tc_fused2_kernel<CG2>, (int)g.smem_bytes);
+    if (e != cudaSuccess) return e;
     const int grid = g.ntiles < device_sm_count() ? g.ntiles : device_sm_count();
     conv_tc_fused2_kernel<CG2><<<grid, fz::NTHREADS, g.smem_bytes, st>>>(
         tm, a.w1, a.b1, a.act1, a.w2, a.b2, a.act2, a.y, a.H, a.W, a.C0, a.C2, g, device_status_ptr(), 1000000000ull);

@@ -4,6 +4,9 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <mutex>
+
 namespace sc {
 
 struct ConvArgs {
@@ -76,6 +79,51 @@ cudaError_t launch_conv_tuned(const ConvArgs &a, cudaStream_t st);
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
+
+// Per-device launch caches of one kernel, safe to use from several host
+// threads at once: the largest dynamic shared memory the kernel has been
+// opted in to (it only grows, so a size below it stays valid), and the
+// resident CTAs per SM of the last size queried, as (smem << 32) | CTAs.
+// Static storage zero-initialises them.
+struct KernelCache {
+    std::atomic<int> allowed[64];
+    std::atomic<long long> occ[64];
+};
+
+// Serialises the cudaFuncSetAttribute calls of every launcher (api.cu).
+std::mutex &launch_cache_mutex();
+
+// Opts `kernel` in to `smem` bytes of dynamic shared memory on device dev
+// (0 <= dev < 64), once per size increase.
+template <class K>
+cudaError_t ensure_dynamic_smem(KernelCache &c, int dev, K kernel, int smem)
+{
+    if (smem <= 48 * 1024 || c.allowed[dev].load(std::memory_order_acquire) >= smem) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(launch_cache_mutex());
+    if (c.allowed[dev].load(std::memory_order_relaxed) >= smem) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) c.allowed[dev].store(smem, std::memory_order_release);
+    return e;
+}
+
+// Resident CTAs per SM of `kernel` with `threads` threads and `smem` bytes
+// of dynamic shared memory on device dev (at least 1).
+template <class K>
+cudaError_t resident_ctas(KernelCache &c, int dev, K kernel, int threads, int smem, int *ctas)
+{
+    const long long v = c.occ[dev].load(std::memory_order_acquire);
+    if (v != 0 && (int)(v >> 32) == smem) {
+        *ctas = (int)(v & 0xffffffffLL);
+        return cudaSuccess;
+    }
+    int b = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, threads, smem);
+    if (e != cudaSuccess) return e;
+    if (b < 1) b = 1;
+    c.occ[dev].store(((long long)smem << 32) | b, std::memory_order_release);
+    *ctas = b;
+    return cudaSuccess;
+}
 
 // Stream-ordered temporary buffers (api.cu) from a library-private memory
 // pool of the current device; see sc_release_workspace.
