@@ -29,6 +29,11 @@ cudaError_t launch_conv_general_k7(const ConvArgs &a, cudaStream_t st);
 // where it does not apply.
 cudaError_t launch_conv_tma_k3_narrow(const ConvArgs &a, cudaStream_t st);
 cudaError_t launch_conv_tma_k3_wide(const ConvArgs &a, cudaStream_t st);
+// The same kernel for 5 x 5 filters with 16 or fewer output channels and for
+// 1 x 1 filters (conv_tma_k5.cu, conv_tma_k1.cu).
+cudaError_t launch_conv_tma_k5_narrow(const ConvArgs &a, cudaStream_t st);
+cudaError_t launch_conv_tma_k1_narrow(const ConvArgs &a, cudaStream_t st);
+cudaError_t launch_conv_tma_k1_wide(const ConvArgs &a, cudaStream_t st);
 // Test hook (sc_test_conv_wait_expiry): the default configuration with
 // copy `drop_copy` of every CTA never issued and waits bounded by timeout_ns.
 cudaError_t launch_conv_tma_k3_test(const ConvArgs &a, int drop_copy, unsigned long long timeout_ns,

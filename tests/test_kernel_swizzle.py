@@ -222,7 +222,7 @@ def test_tma_stage_pixel_reads_conflict_free(swz, cfg):
     F_T = 8 if F_TB >= 8 else 4
     T_X = F_TB // F_T
     CB, PXB = C_SH // 4, 4 * C_SH
-    for j in range(W_T + 2):
+    for j in range(W_T + 6):   # the window of up to 7 x 7 filters
         for cb in range(CB):
             chunks = []
             for lane in range(32):

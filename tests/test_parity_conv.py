@@ -74,6 +74,14 @@ SHAPES = [
     (1, 8, 16, 12, 40, 7, 7),
     (1, 8, 8, 12, 17, 3, 5),
     (1, 8, 8, 12, 17, 7, 1),
+    # TMA-staged 5x5 and 1x1: wide, narrow with Cin % 8 != 0, 16-channel
+    # groups, a filter bank above the TMA kernel's limit (cp.async fallback)
+    (1, 32, 32, 21, 90, 5, 5),
+    (2, 12, 4, 9, 170, 5, 5),
+    (1, 16, 16, 7, 33, 5, 5),
+    (1, 64, 40, 8, 30, 5, 5),
+    (1, 32, 64, 9, 50, 1, 1),
+    (2, 8, 4, 5, 7, 1, 1),
     (2, 4, 36, 5, 9, 5, 3),
 ]
 
