@@ -6,6 +6,8 @@ import sys
 import bench
 import synthetic as S
 
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
 
 def test_kernel_sources_exist():
     for cid in (2, 3, 4):
@@ -38,3 +40,34 @@ def test_oracle_per_config_covers_every_workload():
         assert ("1 thread" in ent) == (name in ("1", "2", "5"))
         if name != "5":
             assert ent["openmp"]["gflops"] > 0
+
+
+def test_profile_commands_use_existing_bench_options():
+    """Every ncu summary under profiles/ names its command; the bench cases
+    and flags it uses must still exist, and the command carries
+    --clock-control none."""
+    import glob
+    flags = {"--steps", "--warmup", "--only", "--no-cpu-baseline", "--no-per-config", "--no-autotune", "--gpus",
+             "--impl"}
+    seen = 0
+    for path in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        text = open(path).read()
+        lines = text.split("\n")
+        for i, line in enumerate(lines):
+            if not line.lstrip().startswith("ncu --"):
+                continue
+            cmd = line
+            k = i
+            while cmd.rstrip().endswith("\\") and k + 1 < len(lines):
+                k += 1
+                cmd = cmd.rstrip()[:-1] + " " + lines[k]
+            assert "--clock-control none" in cmd, path
+            assert "python bench.py" in cmd, path
+            tail = cmd.split("python bench.py", 1)[1].split()
+            for tok in tail:
+                if tok.startswith("--"):
+                    assert tok in flags, (path, tok)
+            if "--only" in tail:
+                assert tail[tail.index("--only") + 1] in bench.ONLY_CASES, path
+            seen += 1
+    assert seen >= 10
