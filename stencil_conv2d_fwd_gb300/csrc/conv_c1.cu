@@ -25,6 +25,11 @@
 // g*4*CL + 4*cl + e, g in {0,1}) so one warp store writes 4*CL contiguous
 // NHWC channels of each of its pixels.  Filters of an R x S kernel sit centred in a
 // K x K register window (K = max(R, S), zero taps around them).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -290,13 +295,22 @@ __global__ void __launch_bounds__(256)
 // The accumulators start at the bias (the sum's first term instead of its
 // last; the rounding stays within the FP32 bound), read from shared memory
 // with the filters, and the stores need one in-image test per thread.
-template <int K, int F_T, int CL>
+// TMA_OUT (32 output channels per CTA): a warp writes its output row (32
+// pixels x 32 channels, 128-byte pixel rows with the 128-byte swizzle) into
+// one of its two shared-memory buffers and lane 0 stores it with one TMA
+// copy (pixels past W and channels past Cout clipped by the copy), so the
+// global stores leave the load/store unit's data pipe, which the filter
+// loads also use.
+template <int K, int F_T, int CL, bool TMA_OUT>
 __global__ void __launch_bounds__(256, (K >= 7 && F_T >= 8) ? 1 : 2)
     conv_c1_ring_kernel(const float *__restrict__ x, const float *__restrict__ w,
                         const float *__restrict__ bias, float *__restrict__ y, int N, int H, int W,
-                        int Cout, int R, int S, int act, int rows_per_cta, int col_tiles)
+                        int Cout, int R, int S, int act, int rows_per_cta, int col_tiles,
+                        const __grid_constant__ CUtensorMap tmy)
 {
     using C = C1Cfg<K, F_T, CL>;
+    static_assert(!TMA_OUT || (F_T == 8 && CL == 4), "TMA stores: 32 channels (128-byte pixel rows) per CTA");
+    extern __shared__ __align__(1024) unsigned char c1_out_raw[];
     __shared__ __align__(16) float ws[K * K * C::CO_CTA];
     __shared__ __align__(16) float bs[C::CO_CTA];
 
@@ -419,7 +433,34 @@ __global__ void __launch_bounds__(256, (K >= 7 && F_T >= 8) ? 1 : 2)
                 }
             }
             raw_c = raw_n;
-            if (px_ok) {
+            if constexpr (TMA_OUT) {
+                // buffer i % 2 of this warp (1024-byte aligned, 4 KB)
+                const uint32_t raw_u = smem_u32(c1_out_raw);
+                const uint32_t buf = ((raw_u + 1023) & ~1023u) + (uint32_t)((warp * 2 + (i & 1)) * 4096);
+                const int xw = (ct * nwarps + warp) * (C::PL * 4);   // the warp's first pixel
+                if (lane == 0) bulk_wait_read<1>();   // the store that last read this buffer is done
+                __syncwarp();
+                if (px_ok) {
+#pragma unroll
+                    for (int g = 0; g < F_T / 4; ++g)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int p = 4 * pl + j;          // pixel of the warp's row
+                            const int q = g * 4 + cl;          // 16-byte chunk: channels 4q .. 4q + 3
+                            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(
+                                             buf + p * 128 + ((q ^ (p & 7)) << 4)),
+                                         "f"(relu_if(acc[4 * g + 0][j], act)), "f"(relu_if(acc[4 * g + 1][j], act)),
+                                         "f"(relu_if(acc[4 * g + 2][j], act)), "f"(relu_if(acc[4 * g + 3][j], act))
+                                         : "memory");
+                        }
+                }
+                fence_proxy_async_smem();   // these writes -> visible to the copy
+                __syncwarp();
+                if (lane == 0 && xw < W) {
+                    tma_store_4d(&tmy, buf, co0, xw, oy, n);
+                    bulk_commit();
+                }
+            } else if (px_ok) {
                 float *yrow = y + ((long long)n * H + oy) * W * Cout;
                 if constexpr (F_T >= 4) {
 #pragma unroll
@@ -447,6 +488,44 @@ __global__ void __launch_bounds__(256, (K >= 7 && F_T >= 8) ? 1 : 2)
             }
         }
     }
+    if constexpr (TMA_OUT)
+        if (lane == 0) bulk_wait_all();   // every store has written global memory
+}
+
+// The driver's tensor-map encoder (conv_tma_k3.cu), or nullptr.
+PFN_cuTensorMapEncodeTiled_v12000 conv_tma_encoder();
+
+// Output rows stored by TMA copies (32 channels per CTA, see the kernel).
+constexpr bool kC1TmaStores = true;
+
+template <int K, int F_T, int CL>
+static cudaError_t launch_c1_tma_out(const ConvArgs &a, cudaStream_t st, dim3 grid, int nwarps, int rows_per_cta,
+                                     int col_tiles)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 encode = conv_tma_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    // NHWC output as (C, W, H, N); box = 32 channels x 32 pixels of one row
+    CUtensorMap tm;
+    const cuuint64_t dims[4] = {(cuuint64_t)a.Cout, (cuuint64_t)a.W, (cuuint64_t)a.H, (cuuint64_t)a.N};
+    const cuuint64_t strides[3] = {(cuuint64_t)a.Cout * 4, (cuuint64_t)a.W * a.Cout * 4,
+                                   (cuuint64_t)a.H * a.W * a.Cout * 4};
+    const cuuint32_t box[4] = {32, 32, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (encode(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.y, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorNotSupported;
+    const int smem = nwarps * 2 * 4096 + 1024;   // two 4 KB row buffers per warp + alignment slack
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    static KernelCache cache;
+    e = ensure_dynamic_smem(cache, dev, conv_c1_ring_kernel<K, F_T, CL, true>, smem);
+    if (e != cudaSuccess) return e;
+    conv_c1_ring_kernel<K, F_T, CL, true><<<grid, nwarps * 32, smem, st>>>(
+        a.x, a.w, a.b, a.y, a.N, a.H, a.W, a.Cout, a.R, a.S, a.act, rows_per_cta, col_tiles, tm);
+    return cudaGetLastError();
 }
 
 template <int K, int F_T, int CL>
@@ -474,10 +553,19 @@ static cudaError_t launch_c1_cfg(const ConvArgs &a, cudaStream_t st)
                     ((reinterpret_cast<uintptr_t>(a.y) & 15) == 0);
     // the ring needs more registers than 7 x 7 filters with 8 channels per
     // thread leave at 2 CTAs per SM; those keep the shifting window
-    if (vec && !(K >= 7 && F_T >= 8))
-        conv_c1_ring_kernel<K, F_T, CL><<<dim3((unsigned)nb, groups, a.N), nwarps * 32, 0, st>>>(
-            a.x, a.w, a.b, a.y, a.N, a.H, a.W, a.Cout, a.R, a.S, a.act, rows_per_cta, col_tiles);
-    else
+    if (vec && !(K >= 7 && F_T >= 8)) {
+        if constexpr (F_T == 8 && CL == 4) {
+            if (kC1TmaStores) {
+                const cudaError_t e = launch_c1_tma_out<K, F_T, CL>(a, st, dim3((unsigned)nb, groups, a.N), nwarps,
+                                                                    rows_per_cta, col_tiles);
+                if (e != cudaErrorNotSupported) return e;
+            }
+        }
+        CUtensorMap unused;
+        std::memset(&unused, 0, sizeof(unused));
+        conv_c1_ring_kernel<K, F_T, CL, false><<<dim3((unsigned)nb, groups, a.N), nwarps * 32, 0, st>>>(
+            a.x, a.w, a.b, a.y, a.N, a.H, a.W, a.Cout, a.R, a.S, a.act, rows_per_cta, col_tiles, unused);
+    } else
         conv_c1_kernel<K, F_T, CL><<<dim3((unsigned)nb, groups, a.N), nwarps * 32, 0, st>>>(
             a.x, a.w, a.b, a.y, a.N, a.H, a.W, a.Cout, a.R, a.S, a.act, rows_per_cta, col_tiles, vec);
     return cudaGetLastError();
