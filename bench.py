@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--no-autotune", action="store_true", help="default tile configurations (no first-call tuning)")
     ap.add_argument("--only", choices=sorted(ONLY_CASES),
                     help="launch one workload's kernel warmup+steps times and exit (for ncu captures)")
+    ap.add_argument("--candidate", type=int, default=None,
+                    help="with --only on a 3x3 FP32 layer: that tile configuration of the autotuner's list")
     return ap.parse_args()
 
 
@@ -800,6 +802,9 @@ def run_only(args, local):
             yb = torch.empty(N * H * W * L.cout, dtype=torch.bfloat16, device=dev)
             launch = lambda: sc.conv2d_fwd_tc_bf16(xb, wd, bd, yb, N, H, W, L.cin, L.cout, L.r, L.s, L.act,
                                                    sc.SC_BF16)
+        elif args.candidate is not None:   # one tile configuration of the autotuner's list
+            launch = lambda: sc.sc_test_conv_candidate(x, wd, bd, y, N, H, W, L.cin, L.cout, L.r, L.s, L.act,
+                                                       args.candidate)
         else:
             launch = lambda: sc.conv2d_fwd(x, wd, bd, y, N, H, W, L.cin, L.cout, L.r, L.s, sc.SC_NHWC, L.act)
     for _ in range(args.warmup + args.steps):

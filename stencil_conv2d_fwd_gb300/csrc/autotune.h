@@ -26,6 +26,7 @@ cudaError_t k3_tma_f4_w3_h4_pc(const ConvArgs &a, cudaStream_t st);
 cudaError_t k3_tma_f4_w5_h8r2(const ConvArgs &a, cudaStream_t st);
 cudaError_t k3_tma_f8_w5_h4(const ConvArgs &a, cudaStream_t st);
 cudaError_t k3_tma_f16_w5_h4(const ConvArgs &a, cudaStream_t st);
+cudaError_t k3_tma_f16_w3_h4(const ConvArgs &a, cudaStream_t st);
 cudaError_t k3_tma_f32_w7_h8(const ConvArgs &a, cudaStream_t st);
 cudaError_t k3_tma_f32_w5_h8(const ConvArgs &a, cudaStream_t st);
 cudaError_t k3_tma_f64_w7_h8(const ConvArgs &a, cudaStream_t st);

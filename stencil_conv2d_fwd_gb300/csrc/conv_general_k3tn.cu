@@ -20,6 +20,7 @@ static const TuneCand k3_n16[] = {
     {"F16 W8 4x128", cand_n<16, 8, 4, 128, 2>},
     {"F16 W4 8x64", cand_n<16, 4, 8, 64, 1>},
     {"TMA F16 W5 4x80", k3_tma_f16_w5_h4},
+    {"TMA F16 W3 4x48", k3_tma_f16_w3_h4},
 };
 static const TuneCand k3_n8[] = {
     {"heuristic", launch_conv_general_k3},

@@ -52,6 +52,10 @@ cudaError_t k3_tma_f16_w5_h4(const ConvArgs &a, cudaStream_t st)
 {
     return launch_conv_tma<TmaCfg<3, 16, 5, 4, 1, 8, 3, 2, false>>(a, st);
 }
+cudaError_t k3_tma_f16_w3_h4(const ConvArgs &a, cudaStream_t st)
+{
+    return launch_conv_tma<TmaCfg<3, 16, 3, 4, 1, 8, 2, 2, false>>(a, st);
+}
 cudaError_t k3_tma_f32_w7_h8(const ConvArgs &a, cudaStream_t st)
 {
     return launch_conv_tma<TmaCfg<3, 32, 7, 8, 1, 8, 3, 1, false>>(a, st);
@@ -93,6 +97,11 @@ cudaError_t launch_conv_tma_k3_narrow(const ConvArgs &a, cudaStream_t st)
 {
     if (a.Cout <= 4) return k3_tma_f4_w5_h4(a, st);
     if (a.Cout <= 8) return k3_tma_f8_w5_h4(a, st);
+    // 9-16 channels: 80 x 4 pixel tiles; where those give fewer tiles than
+    // the device has SMs, 48 x 4 tiles spread the work over more SMs
+    // (16 -> 16 on 128 x 128: 12.9 -> 10.9 us a call)
+    const long long tiles80 = (long long)((a.W + 79) / 80) * ((a.H + 3) / 4) * a.N;
+    if (tiles80 < device_sm_count()) return k3_tma_f16_w3_h4(a, st);
     return k3_tma_f16_w5_h4(a, st);
 }
 

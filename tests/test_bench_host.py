@@ -48,7 +48,7 @@ def test_profile_commands_use_existing_bench_options():
     --clock-control none."""
     import glob
     flags = {"--steps", "--warmup", "--only", "--no-cpu-baseline", "--no-per-config", "--no-autotune", "--gpus",
-             "--impl"}
+             "--impl", "--candidate"}
     seen = 0
     for path in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
         text = open(path).read()

@@ -63,6 +63,7 @@ SHAPES = [
     (2, 8, 8, 9, 13, 3, 3),
     (1, 12, 20, 17, 70, 3, 3),
     (3, 16, 16, 33, 65, 3, 3),
+    (2, 32, 12, 10, 101, 3, 3),   # 9-16 channels on a small image: 48-pixel tiles
     (1, 32, 32, 19, 131, 3, 3),
     (1, 32, 4, 11, 300, 3, 3),
     (2, 64, 64, 15, 57, 3, 3),
