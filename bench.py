@@ -45,6 +45,7 @@ ONLY_CASES = {
     "1": (1, 0), "2": (2, 0), "3-L1": (3, 0), "3-L2": (3, 1), "3-L3": (3, 2), "4": (4, 0), "5": (5, None),
     "4-tc": (4, 0), "3-L2-tc": (3, 1), "3-L3-tc": (3, 2),
     "4-bf16": (4, 0), "3-L2-bf16": (3, 1), "3-L3-bf16": (3, 2), "3-L23-fused": (3, 1),
+    "4-x3": (4, 0), "3-L2-x3": (3, 1), "3-L3-x3": (3, 2),
 }
 
 
@@ -490,35 +491,44 @@ def per_config(sc, S, dev, stream, flush, fp32_tflops, hbm_gbs, hbm_src):
     c4 = S.config(4)
     conv_entry("4: N=32 56x56 64->64 3x3", 32, 56, 56, c4.layers[0], c4.x.transpose(0, 2, 3, 1))
 
-    # tensor-core (tcgen05, TF32) variant, reported separately: its own
-    # tolerance (5e-3 * sum|x*w|) and its own roofline (TF32 tensor peak)
+    # tensor-core (tcgen05) variants, reported separately, each against the
+    # TF32 tensor peak and HBM:
+    #  * conv2d_fwd_tc: TF32 operands, its own tolerance (5e-3 * sum|x*w|);
+    #  * conv2d_fwd_tc_x3: split TF32 (three TF32 products per product), the
+    #    fp32 tolerance (1e-5 * sum|x*w|); its tensor work is 3x the FLOPs.
     peaks = measured_peaks() or {}
     tf32_tflops = float(peaks.get("bf16_tflops", 1900.0)) * 1.1 / 2.25
-    for name, cid, li in (("4 (tcgen05 TF32)", 4, 0), ("3-L2 (tcgen05 TF32)", 3, 1), ("3-L3 (tcgen05 TF32)", 3, 2)):
-        wl = S.config(cid)
-        L = wl.layers[li]
-        xin = wl.x if li == 0 else np.maximum(S.uniform(77, 0, (wl.n, L.cin, wl.h, wl.w), -1, 1), 0)
-        xd = torch.from_numpy(np.ascontiguousarray(xin.transpose(0, 2, 3, 1)).astype(np.float32)).to(dev)
-        wd, bd = torch.from_numpy(L.w).to(dev), torch.from_numpy(L.b).to(dev)
-        yd = torch.empty(wl.n * wl.h * wl.w * L.cout, device=dev)
+    variants = (("tcgen05 TF32", sc.conv2d_fwd_tc, 1, "5e-3 * sum|x*w| (TF32 operands)"),
+                ("tcgen05 split TF32", sc.conv2d_fwd_tc_x3, 3,
+                 "1e-5 * sum|x*w| (fp32 bound; x = hi + lo, w = hi + lo, three TF32 products)"))
+    for vname, entry, work, tol in variants:
+        for cname, cid, li in (("4", 4, 0), ("3-L2", 3, 1), ("3-L3", 3, 2)):
+            wl = S.config(cid)
+            L = wl.layers[li]
+            xin = wl.x if li == 0 else np.maximum(S.uniform(77, 0, (wl.n, L.cin, wl.h, wl.w), -1, 1), 0)
+            xd = torch.from_numpy(np.ascontiguousarray(xin.transpose(0, 2, 3, 1)).astype(np.float32)).to(dev)
+            wd, bd = torch.from_numpy(L.w).to(dev), torch.from_numpy(L.b).to(dev)
+            yd = torch.empty(wl.n * wl.h * wl.w * L.cout, device=dev)
 
-        def call_tc(s=None):
-            rc = sc.conv2d_fwd_tc(xd, wd, bd, yd, wl.n, wl.h, wl.w, L.cin, L.cout, L.r, L.s, L.act,
-                                  s if s is not None else stream)
-            if rc != 0:
-                raise RuntimeError(sc.sc_status_string(rc))
-        med, mn = time_events(call_tc, stream, flush, reps=20)
-        flops = conv_flops(wl.n, wl.h, wl.w, L)
-        byts = 4 * (wl.n * wl.h * wl.w * (L.cin + L.cout) + L.w.size + L.b.size)
-        t_c, t_m = flops / (tf32_tflops * 1e12), byts / (hbm_gbs * 1e9)
-        out[name] = {"ms_median": round(med, 5), "ms_min": round(mn, 5),
-                     "gflops": round(flops / (med * 1e-3) / 1e9, 2),
-                     "mpixel_per_s": round(wl.n * wl.h * wl.w / (med * 1e-3) / 1e6, 2),
-                     "roofline_bound": "tensor" if t_c >= t_m else "hbm",
-                     "roofline_us": round(max(t_c, t_m) * 1e6, 3),
-                     "roofline_frac": round(max(t_c, t_m) / (med * 1e-3), 4),
-                     "tolerance": "5e-3 * sum|x*w| (TF32 operands)",
-                     "tf32_peak_tflops": round(tf32_tflops, 1)}
+            def call_tc(s=None):
+                rc = entry(xd, wd, bd, yd, wl.n, wl.h, wl.w, L.cin, L.cout, L.r, L.s, L.act,
+                           s if s is not None else stream)
+                if rc != 0:
+                    raise RuntimeError(sc.sc_status_string(rc))
+            med, mn = time_events(call_tc, stream, flush, reps=20)
+            flops = conv_flops(wl.n, wl.h, wl.w, L)
+            byts = 4 * (wl.n * wl.h * wl.w * (L.cin + L.cout) + L.w.size + L.b.size)
+            t_c, t_m = work * flops / (tf32_tflops * 1e12), byts / (hbm_gbs * 1e9)
+            out[f"{cname} ({vname})"] = {
+                "ms_median": round(med, 5), "ms_min": round(mn, 5),
+                "gflops": round(flops / (med * 1e-3) / 1e9, 2),
+                "mpixel_per_s": round(wl.n * wl.h * wl.w / (med * 1e-3) / 1e6, 2),
+                "roofline_bound": "tensor" if t_c >= t_m else "hbm",
+                "roofline_us": round(max(t_c, t_m) * 1e6, 3),
+                "roofline_frac": round(max(t_c, t_m) / (med * 1e-3), 4),
+                "tolerance": tol,
+                "tensor_flops_per_fp32_flop": work,
+                "tf32_peak_tflops": round(tf32_tflops, 1)}
 
     # bf16 activation storage with BF16 tensor-core operands (conv2d_fwd_tc_bf16):
     # x and y bf16 in HBM (the synthetic input rounded to bf16), fp32 filters and
@@ -791,6 +801,8 @@ def run_only(args, local):
                 x = y
         if args.only.endswith("-tc"):   # the tensor-core (TF32) variant
             launch = lambda: sc.conv2d_fwd_tc(x, wd, bd, y, N, H, W, L.cin, L.cout, L.r, L.s, L.act)
+        elif args.only.endswith("-x3"):   # the split-TF32 tensor-core variant
+            launch = lambda: sc.conv2d_fwd_tc_x3(x, wd, bd, y, N, H, W, L.cin, L.cout, L.r, L.s, L.act)
         elif args.only == "3-L23-fused":   # layers 2 and 3 fused on the tensor cores
             L3 = wl.layers[2]
             w3d, b3d = torch.from_numpy(L3.w).to(dev), torch.from_numpy(L3.b).to(dev)

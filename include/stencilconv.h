@@ -101,6 +101,26 @@ int conv2d_fwd_tc(const float *x, const float *w, const float *b, float *y,
                   int act, sc_stream_t stream);
 
 /*
+ * conv2d_fwd_tc_x3: conv2d_fwd_tc with fp32-level accuracy: every operand v
+ * is split into a TF32 head hi(v) (v with its 13 low mantissa bits cleared)
+ * and a remainder lo(v) = v - hi(v), and each product x * w is computed on
+ * the tensor cores as hi(x) hi(w) + hi(x) lo(w) + lo(x) hi(w), the last two
+ * in a separate accumulator added once at the end (split or "3xTF32"
+ * arithmetic: Ootomo and Yokota, "Recovering single precision accuracy from
+ * Tensor Cores while surpassing the FP32 theoretical peak performance",
+ * 2022).  The dropped lo(x) lo(w) and the remainders' own TF32 rounding keep
+ * every product within about 3 * 2^-20 of exact, so the result meets
+ * conv2d_fwd's bound |y - y_ref| <= 1e-5 * (sum|x * w| + |b|).  Three MMAs
+ * per product: a separate variant, not conv2d_fwd's FP32 FMA path.
+ * Arguments, layouts and errors as for conv2d_fwd_tc.  Both the filters'
+ * heads and remainders stay resident in shared memory, so the supported
+ * Cin is about half of conv2d_fwd_tc's (about 250).
+ */
+int conv2d_fwd_tc_x3(const float *x, const float *w, const float *b, float *y,
+                     int N, int H, int W, int Cin, int Cout, int R, int S,
+                     int act, sc_stream_t stream);
+
+/*
  * conv2d_fwd_tc_bf16: conv2d_fwd_tc with bf16 activation storage and BF16
  * tensor-core operands (tcgen05 kind::f16), fp32 accumulation.  Storing
  * activations in 16-bit floats halves their bytes ("Optimizing convolution

@@ -39,6 +39,7 @@ _I = ctypes.c_int
 SIGNATURES = {
     "conv2d_fwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "conv2d_fwd_tc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
+    "conv2d_fwd_tc_x3": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "conv2d_fwd_tc_bf16": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "conv2d_fwd_tc_fused2": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "stencil_pipeline_fwd": (_I, [_P, _P, _I, _I, _P]),
@@ -118,6 +119,12 @@ def conv2d_fwd_tc(x, w, b, y, N, H, W, Cin, Cout, R, S, act=SC_ACT_NONE, stream=
     """Tensor-core (TF32) variant of conv2d_fwd, NHWC only (see the header)."""
     return load().conv2d_fwd_tc(_ptr(x), _ptr(w), _ptr(b), _ptr(y), N, H, W, Cin, Cout, R, S, act,
                                 _stream(stream))
+
+
+def conv2d_fwd_tc_x3(x, w, b, y, N, H, W, Cin, Cout, R, S, act=SC_ACT_NONE, stream=None) -> int:
+    """conv2d_fwd_tc with split-TF32 operands, fp32-level results (see the header)."""
+    return load().conv2d_fwd_tc_x3(_ptr(x), _ptr(w), _ptr(b), _ptr(y), N, H, W, Cin, Cout, R, S, act,
+                                   _stream(stream))
 
 
 def conv2d_fwd_tc_bf16(x, w, b, y, N, H, W, Cin, Cout, R, S, act=SC_ACT_NONE, y_dtype=SC_BF16,

@@ -222,8 +222,10 @@ int conv2d_fwd(const float *x, const float *w, const float *b, float *y, int N, 
     return rc;
 }
 
-int conv2d_fwd_tc(const float *x, const float *w, const float *b, float *y, int N, int H, int W, int Cin,
-                  int Cout, int R, int S, int act, sc_stream_t stream)
+// The argument checks shared by conv2d_fwd_tc and conv2d_fwd_tc_x3; SC_OK
+// when the call may launch.
+static int check_tc_args(const float *x, const float *w, const float *b, const float *y, int N, int H, int W,
+                         int Cin, int Cout, int R, int S, int act)
 {
     if (!x || !w || !y) return SC_ERR_NULL;
     const long long nx = checked_count({N, H, W, Cin});
@@ -240,6 +242,25 @@ int conv2d_fwd_tc(const float *x, const float *w, const float *b, float *y, int 
         overlaps(y, ybytes, w, (size_t)nw * sizeof(float)) ||
         overlaps(y, ybytes, b, b ? (size_t)Cout * sizeof(float) : 0))
         return SC_ERR_ALIAS;
+    return SC_OK;
+}
+
+int conv2d_fwd_tc_x3(const float *x, const float *w, const float *b, float *y, int N, int H, int W, int Cin,
+                     int Cout, int R, int S, int act, sc_stream_t stream)
+{
+    const int chk = check_tc_args(x, w, b, y, N, H, W, Cin, Cout, R, S, act);
+    if (chk != SC_OK) return chk;
+    sc::ConvArgs a{x, w, b, y, N, H, W, Cin, Cout, R, S, act};
+    const cudaError_t e = sc::launch_conv_tc_x3(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return SC_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? SC_OK : cuda_fail(e);
+}
+
+int conv2d_fwd_tc(const float *x, const float *w, const float *b, float *y, int N, int H, int W, int Cin,
+                  int Cout, int R, int S, int act, sc_stream_t stream)
+{
+    const int chk = check_tc_args(x, w, b, y, N, H, W, Cin, Cout, R, S, act);
+    if (chk != SC_OK) return chk;
     sc::ConvArgs a{x, w, b, y, N, H, W, Cin, Cout, R, S, act};
     const cudaError_t e = sc::launch_conv_tc(a, reinterpret_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported) return SC_ERR_UNSUPPORTED;

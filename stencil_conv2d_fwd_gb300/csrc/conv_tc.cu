@@ -81,6 +81,8 @@ constexpr int MAX_STAGE = 6;
 constexpr int TMEM_BUF = 256;   // tensor-memory columns per accumulator buffer (two buffers)
 constexpr int OUT_BUF = 4096;                // one epilogue output buffer: 30 pixel rows of up to 128 bytes
 constexpr int STG_BYTES = 8 * OUT_BUF;       // one per epilogue warp
+constexpr int X3_LO = 2;                     // split TF32: buffers for the stages' remainders (a ring of its own)
+constexpr int X3_STG_BYTES = 4 * OUT_BUF;    // split TF32: four epilogue warps
 
 struct TcGeom {
     int MT, TR, THh;                // M-tiles per tile, tile rows (4 * MT), staged rows (TR + 2)
@@ -112,8 +114,13 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
     constexpr int OROWB = CW * OSZ;                // bytes of one pixel's group of outputs
     constexpr bool TMA_OUT = OROWB >= 64;          // store through a swizzled shared-memory buffer and TMA
     constexpr int OCH = OROWB >= 16 ? OROWB / 16 : 1;   // 16-byte chunks per pixel (or one 8-byte piece)
+    constexpr bool X3 = OP::X3;                    // split TF32: head and correction accumulators
+    constexpr int DSTR = X3 ? 2 * NB : NB;         // tensor-memory columns per M-tile
+    constexpr int RB = X3 ? 2 * NB : NB;           // filter-bank rows per (K step, tap, 4-channel block)
     extern __shared__ __align__(1024) unsigned char smem_dyn[];
     __shared__ __align__(8) unsigned long long full_bar[tc::MAX_STAGE], empty_bar[tc::MAX_STAGE];
+    __shared__ __align__(8) unsigned long long conv_bar[X3 ? tc::MAX_STAGE : 1];   // X3: a stage is split
+    __shared__ __align__(8) unsigned long long lo_empty[X3 ? tc::X3_LO : 1];       // X3: a remainder buffer is free
     __shared__ __align__(8) unsigned long long acc_full[2], acc_empty[2], w_bar, wt_bar;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
@@ -124,8 +131,11 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
     const int ns = g.nstage;
     // stage buffers need 1024-byte alignment (the 128-byte swizzle pattern)
     unsigned char *smem_raw = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
-    unsigned char *abuf = smem_raw;                      // ns activation stages
-    unsigned char *wsm = abuf + (size_t)ns * g.stage_bytes;   // resident filters
+    unsigned char *abuf = smem_raw;                      // ns activation stages (X3: their TF32 heads)
+    // X3: X3_LO buffers for the remainders, same layout as a stage; stage j
+    // (head buffer j % ns) puts its remainders in buffer j % X3_LO
+    unsigned char *alo = abuf + (size_t)ns * g.stage_bytes;
+    unsigned char *wsm = alo + (X3 ? (size_t)tc::X3_LO * g.stage_bytes : 0);   // resident filters (X3: heads and remainders)
     unsigned char *stg = wsm + g.w_bytes;                // epilogue transpose buffers
 
     // Filters, once per CTA.  The producer warp bulk-copies the group's OIHW
@@ -152,9 +162,13 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
             mbar_init(smem_u32(&full_bar[j]), 1);
             mbar_init(smem_u32(&empty_bar[j]), 1);
         }
+        if constexpr (X3) {
+            for (int j = 0; j < ns; ++j) mbar_init(smem_u32(&conv_bar[j]), 4);   // one arrive per converting warp
+            for (int j = 0; j < tc::X3_LO; ++j) mbar_init(smem_u32(&lo_empty[j]), 1);
+        }
         for (int j = 0; j < 2; ++j) {
             mbar_init(smem_u32(&acc_full[j]), 1);
-            mbar_init(smem_u32(&acc_empty[j]), 8);   // one arrive per epilogue warp
+            mbar_init(smem_u32(&acc_empty[j]), X3 ? 4 : 8);   // one arrive per epilogue warp
         }
         mbar_init(smem_u32(&w_bar), 1);
         mbar_init(smem_u32(&wt_bar), tc::NTHREADS / 32 - 1);   // every warp but the producer
@@ -242,14 +256,30 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
             constexpr uint32_t AR = 2 * OP::ROWB, AM = 8 * OP::ROWB;   // A units per vertical tap (32 rows), per M-tile (128 rows)
             const uint32_t asub = (g.stage_bytes / OP::SUB) >> 4;         // A units per sub-buffer
             const uint32_t a_base = smem_u32(abuf) >> 4, w_base = smem_u32(wsm) >> 4;
-            const uint32_t a_lbo = 1u << 16, b_lbo = (uint32_t)NB << 16;
+            const uint32_t a_lbo = 1u << 16, b_lbo = (uint32_t)RB << 16;
+            // X3: the current stage's remainders, in 16-byte units from its
+            // heads (set per stage; start addresses stay below 2^14 units)
+            uint32_t alo_off = 0;
+            constexpr uint32_t idesc2 = tc::idesc_mma(OP::FMT, 2 * NB);
+            // One (K step, tap, M-tile): the head product into the M-tile's
+            // first NB columns.  X3: x_hi [w_hi | w_lo] (N = 2 NB) puts the
+            // head product and x_hi w_lo side by side, then x_lo w_hi (the
+            // bank's first NB rows) adds into the correction columns.
+            auto mma1 = [&](uint32_t d, uint32_t ad, uint32_t bd, uint32_t acc) {
+                if constexpr (X3) {
+                    tc::mma_w<OP>(d, ad, A_HI, bd, tc::B_HI, idesc2, acc);
+                    tc::mma_w<OP>(d + NB, ad + alo_off, A_HI, bd, tc::B_HI, idesc, 1u);
+                } else {
+                    tc::mma_w<OP>(d, ad, A_HI, bd, tc::B_HI, idesc, acc);
+                }
+            };
             // G M-tiles at a time, M-tiles innermost: consecutive MMAs go to
             // different accumulators (back-to-back MMAs into one accumulator
             // issue more slowly); a full stage (KS K steps) is unrolled so that
             // every descriptor is a register plus a constant.  A: +2 units
             // (32 B) per K step within a row, asub per sub-buffer, AR per
             // vertical tap, AM per M-tile.  B:
-            // 2 * NB units per (K step, tap).
+            // 2 * RB units per (K step, tap).
             auto issue = [&](auto gsz, uint32_t d0, uint32_t a0, uint32_t b0, int nks, uint32_t acc0) {
                 constexpr int G = decltype(gsz)::value;
                 if (nks == KS) {
@@ -259,9 +289,8 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
                         for (int r = 0; r < 3; ++r)
 #pragma unroll
                             for (int gi = 0; gi < G; ++gi)
-                                tc::mma_w<OP>(d0 + (uint32_t)(gi * NB), a0 + (uint32_t)(kk / KSUB) * asub + (uint32_t)((kk % KSUB) * 2 + r * AR + gi * AM),
-                                               A_HI, b0 + (uint32_t)((kk * 3 + r) * 2 * NB), tc::B_HI, idesc,
-                                               (kk > 0 || r > 0) ? 1u : acc0);
+                                mma1(d0 + (uint32_t)(gi * DSTR), a0 + (uint32_t)(kk / KSUB) * asub + (uint32_t)((kk % KSUB) * 2 + r * AR + gi * AM),
+                                     b0 + (uint32_t)((kk * 3 + r) * 2 * RB), (kk > 0 || r > 0) ? 1u : acc0);
                     return;
                 }
 #pragma unroll 1
@@ -270,9 +299,8 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
                     for (int r = 0; r < 3; ++r)
 #pragma unroll
                         for (int gi = 0; gi < G; ++gi)
-                            tc::mma_w<OP>(d0 + (uint32_t)(gi * NB), a0 + (uint32_t)(kk / KSUB) * asub + (uint32_t)((kk % KSUB) * 2 + r * AR + gi * AM),
-                                           A_HI, b0 + (uint32_t)((kk * 3 + r) * 2 * NB), tc::B_HI, idesc,
-                                           (kk > 0 || r > 0) ? 1u : acc0);
+                            mma1(d0 + (uint32_t)(gi * DSTR), a0 + (uint32_t)(kk / KSUB) * asub + (uint32_t)((kk % KSUB) * 2 + r * AR + gi * AM),
+                                 b0 + (uint32_t)((kk * 3 + r) * 2 * RB), (kk > 0 || r > 0) ? 1u : acc0);
                 }
             };
             int s = 0, j = 0, committed = -1;
@@ -288,13 +316,16 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
                 const uint32_t dbase = tmem + (uint32_t)(b * tc::TMEM_BUF);
                 bool ok = true;
                 for (int c = 0; c < g.nstg; ++c, ++j) {
-                    if (!mbar_wait_bounded(smem_u32(&full_bar[s]), ph, timeout_ns)) {
+                    // X3: the stage once its heads and remainders are written
+                    if (!mbar_wait_bounded(smem_u32(X3 ? &conv_bar[s] : &full_bar[s]), ph, timeout_ns)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after_sync();
                     const uint32_t a_lo = (a_base + (uint32_t)s * (g.stage_bytes >> 4)) | a_lbo;
-                    const uint32_t b_lo = (w_base + (uint32_t)(c * KS * 3 * 2 * NB)) | b_lbo;
+                    if constexpr (X3)
+                        alo_off = (uint32_t)(((size_t)(ns - s + j % tc::X3_LO) * g.stage_bytes) >> 4);
+                    const uint32_t b_lo = (w_base + (uint32_t)(c * KS * 3 * 2 * RB)) | b_lbo;
                     const int nks = g.nk - KS * c < KS ? g.nk - KS * c : KS;
                     const uint32_t acc0 = c > 0 ? 1u : 0u;
                     int mt = 0;
@@ -307,9 +338,10 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
                     }
 #pragma unroll 1
                     for (; mt < g.MT; mt += 2)
-                        issue(std::integral_constant<int, 2>{}, dbase + (uint32_t)(mt * NB), a_lo + (uint32_t)(mt * AM),
+                        issue(std::integral_constant<int, 2>{}, dbase + (uint32_t)(mt * DSTR), a_lo + (uint32_t)(mt * AM),
                               b_lo, nks, acc0);
                     tc::mma_commit(smem_u32(&empty_bar[s]));
+                    if constexpr (X3) tc::mma_commit(smem_u32(&lo_empty[j % tc::X3_LO]));
                     committed = j;
                     if (++s == ns) {
                         s = 0;
@@ -326,6 +358,55 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
             if (committed >= 0)
                 (void)mbar_wait_bounded(smem_u32(&empty_bar[committed % ns]), (committed / ns) & 1, timeout_ns);
         }
+    } else if (X3 && warp >= 6) {
+        // ---------------------------------------------------- X3: converters
+        // Warps 6-9 split each landed stage in place: the TF32 heads over the
+        // copied values, the remainders into the stage's twin buffer (the
+        // same offsets, so the same swizzle phase); then the writes are made
+        // visible to the tensor core and the stage goes to the MMA warp.
+        const int ct = tid - 6 * 32;
+        const uint32_t nchunk = g.stage_bytes >> 4;
+        constexpr int CB = 4;   // 16-byte chunks a thread loads before it writes
+        int s = 0;
+        uint32_t ph = 0;
+        for (int j = 0; j < total; ++j) {
+            if (aborted()) break;
+            const int l = j % tc::X3_LO;
+            // the stage has landed, and the MMAs of stage j - X3_LO have read
+            // this remainder buffer
+            bool got = mbar_wait_bounded(smem_u32(&full_bar[s]), ph, timeout_ns);
+            if (got && j >= tc::X3_LO)
+                got = mbar_wait_bounded(smem_u32(&lo_empty[l]), (uint32_t)((j / tc::X3_LO - 1) & 1), timeout_ns);
+            if (__any_sync(0xffffffffu, !got)) {
+                if (lane == 0) give_up();
+                break;
+            }
+            uint4 *hp = reinterpret_cast<uint4 *>(abuf + (size_t)s * g.stage_bytes);
+            uint4 *lp = reinterpret_cast<uint4 *>(alo + (size_t)l * g.stage_bytes);
+            for (uint32_t c0 = (uint32_t)ct; c0 < nchunk; c0 += 128 * CB) {
+                uint4 v[CB];
+#pragma unroll
+                for (int q = 0; q < CB; ++q)
+                    if (c0 + 128 * q < nchunk) v[q] = hp[c0 + 128 * q];
+#pragma unroll
+                for (int q = 0; q < CB; ++q) {
+                    const uint32_t c = c0 + 128 * q;
+                    if (c < nchunk) {
+                        lp[c] = make_uint4(tc::tf32_rest(v[q].x), tc::tf32_rest(v[q].y), tc::tf32_rest(v[q].z),
+                                           tc::tf32_rest(v[q].w));
+                        hp[c] = make_uint4(tc::tf32_head(v[q].x), tc::tf32_head(v[q].y), tc::tf32_head(v[q].z),
+                                           tc::tf32_head(v[q].w));
+                    }
+                }
+            }
+            fence_proxy_async_smem();   // these writes -> visible to the tensor core
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&conv_bar[s]));
+            if (++s == ns) {
+                s = 0;
+                ph ^= 1u;
+            }
+        }
     } else {
         // ------------------------------------------------------------ epilogue
         // Two sets of four warps (0-3 and 6-9); warp w reads TMEM lane
@@ -339,7 +420,9 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
         // previous store to have read the buffer.  Otherwise (outputs of 16
         // or 32 bytes per pixel) each lane stores its pixel directly:
         // neighbouring lanes write neighbouring pixels.
+        // (X3: warps 0-3 only, every M-tile; warps 6-9 convert)
         const int q4 = warp & 3, set = warp < 4 ? 0 : 1;
+        constexpr int MSTEP = X3 ? 1 : 2;
         float bias_r[CW];
 #pragma unroll
         for (int i = 0; i < CW; ++i) bias_r[i] = (bias && co0 + i < Cout) ? __ldg(bias + co0 + i) : 0.f;
@@ -356,31 +439,50 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
             int n, y0, x0;
             tile_origin(u, n, y0, x0);
             const uint32_t tbuf = tmem + (uint32_t)(b * tc::TMEM_BUF) + ((uint32_t)(q4 * 32) << 16);
-            const int last_mt = set + ((g.MT - 1 - set) & ~1);   // this set's last M-tile (< set: none)
+            const int last_mt = X3 ? g.MT - 1 : set + ((g.MT - 1 - set) & ~1);   // this set's last M-tile (< set: none)
             if (last_mt < set) {
                 // nothing of this tile for this warp: release the buffer at once
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&acc_empty[b]));
             }
-            for (int mt = set; mt < g.MT; mt += 2) {
-                uint32_t r0[CW], r1[CW], r2[CW];
-                tc::tmem_ld<CW>(tbuf + (uint32_t)(mt * NB), r0);
-                tc::tmem_ld<CW>(tbuf + (uint32_t)(mt * NB + CG), r1);
-                tc::tmem_ld<CW>(tbuf + (uint32_t)(mt * NB + 2 * CG), r2);
-                tc::tmem_wait_ld();
+            for (int mt = set; mt < g.MT; mt += MSTEP) {
+                // v[i] = sum over s of column (s, i) of lane l + s (X3: heads
+                // plus corrections), in the order s = 0, 1, 2, then the bias
+                float v[CW];
+                if constexpr (X3) {
+#pragma unroll
+                    for (int blk = 0; blk < 3; ++blk) {
+                        uint32_t m[CW], c[CW];
+                        tc::tmem_ld<CW>(tbuf + (uint32_t)(mt * DSTR + blk * CG), m);
+                        tc::tmem_ld<CW>(tbuf + (uint32_t)(mt * DSTR + NB + blk * CG), c);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < CW; ++i) {
+                            float t = __uint_as_float(m[i]) + __uint_as_float(c[i]);
+                            if (blk > 0) t = __shfl_down_sync(0xffffffffu, t, blk);
+                            v[i] = blk == 0 ? t : v[i] + t;
+                        }
+                    }
+                } else {
+                    uint32_t r0[CW], r1[CW], r2[CW];
+                    tc::tmem_ld<CW>(tbuf + (uint32_t)(mt * DSTR), r0);
+                    tc::tmem_ld<CW>(tbuf + (uint32_t)(mt * DSTR + CG), r1);
+                    tc::tmem_ld<CW>(tbuf + (uint32_t)(mt * DSTR + 2 * CG), r2);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < CW; ++i)
+                        v[i] = __uint_as_float(r0[i]) + __shfl_down_sync(0xffffffffu, __uint_as_float(r1[i]), 1) +
+                               __shfl_down_sync(0xffffffffu, __uint_as_float(r2[i]), 2);
+                }
                 if (mt == last_mt) {
                     // every column this warp needs is in registers: release the buffer
                     tc::fence_before_sync();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&acc_empty[b]));
                 }
-                float v[CW];
 #pragma unroll
-                for (int i = 0; i < CW; ++i)
-                    v[i] = relu_if(__uint_as_float(r0[i]) + __shfl_down_sync(0xffffffffu, __uint_as_float(r1[i]), 1) +
-                                       __shfl_down_sync(0xffffffffu, __uint_as_float(r2[i]), 2) + bias_r[i],
-                                   act);
+                for (int i = 0; i < CW; ++i) v[i] = relu_if(v[i] + bias_r[i], act);
                 // the pixel's outputs as 32-bit words: fp32, or bf16 pairs
                 constexpr int NWD = CW * OSZ / 4;
                 uint32_t o[NWD];
@@ -444,13 +546,18 @@ constexpr size_t kTcSmemCap = 227 * 1024 - 1024;
 // fit in shared memory beside the filters and the epilogue buffers; among
 // those, the MT that wastes least work on halo rows, partial tiles and an
 // unevenly filled persistent grid.  Leftover shared memory goes to further
-// stage buffers (up to MAX_STAGE).
+// stage buffers (up to MAX_STAGE).  x3 (split TF32): X3_LO more buffers of a
+// stage's size hold remainders, the filter bank holds heads and remainders
+// (twice the rows), an M-tile takes 2 * NB accumulator columns (heads and
+// corrections), and four epilogue warps need four output buffers.
 static bool tc_geometry(int Cg, int NB, int kc, int rowb, int groups, int Cin, int RS, int H, int W, int Nimg,
-                        tc::TcGeom &g)
+                        bool x3, tc::TcGeom &g)
 {
     const int nk = (Cin + kc - 1) / kc;
-    const size_t w_bytes = ((size_t)nk * 3 * 2 * NB * 16 + 1023) & ~(size_t)1023;
-    const size_t fixed = w_bytes + tc::STG_BYTES + 1024;   // + alignment slack
+    const size_t w_bytes = ((size_t)nk * 3 * 2 * (x3 ? 2 * NB : NB) * 16 + 1023) & ~(size_t)1023;
+    const int cols = x3 ? 2 * NB : NB;   // accumulator columns per M-tile
+    const int nlo = x3 ? tc::X3_LO : 0;  // remainder buffers, each the size of a stage
+    const size_t fixed = w_bytes + (x3 ? tc::X3_STG_BYTES : tc::STG_BYTES) + 1024;   // + alignment slack
     if (fixed >= kTcSmemCap) return false;
     const int sms = device_sm_count() / groups > 0 ? device_sm_count() / groups : 1;   // CTAs per channel group
     const int tiles_x = (W + tc::TC - 1) / tc::TC;
@@ -460,11 +567,11 @@ static bool tc_geometry(int Cg, int NB, int kc, int rowb, int groups, int Cin, i
     // of 16-byte units per output channel
     const int raw_pitch = tc::filter_raw_pitch(Cin, RS);
     const size_t raw = (size_t)Cg * raw_pitch * 16;
-    for (int MT = 1; MT * NB <= tc::TMEM_BUF && MT <= 16; ++MT) {
+    for (int MT = 1; MT * cols <= tc::TMEM_BUF && MT <= 16; ++MT) {
         const int TR = 4 * MT;
         const size_t stage = (size_t)(TR + 2) * tc::WP * rowb;
-        if (fixed + tc::MIN_STAGE * stage > kTcSmemCap) break;
-        const size_t nfit = (kTcSmemCap - fixed) / stage;
+        if (fixed + (tc::MIN_STAGE + nlo) * stage > kTcSmemCap) break;
+        const size_t nfit = (kTcSmemCap - fixed) / stage - nlo;
         if ((nfit < tc::MAX_STAGE ? nfit : tc::MAX_STAGE) * stage < raw) continue;
         const long long tiles = (long long)tiles_x * ((H + TR - 1) / TR) * Nimg;
         const long long rounds = (tiles + sms - 1) / sms;
@@ -488,10 +595,10 @@ static bool tc_geometry(int Cg, int NB, int kc, int rowb, int groups, int Cin, i
     g.nstg = (Cin + tc::CH - 1) / tc::CH;
     g.stage_bytes = (uint32_t)((size_t)g.THh * tc::WP * rowb);
     g.w_bytes = (uint32_t)w_bytes;
-    const int ns = (int)((kTcSmemCap - fixed) / g.stage_bytes);
+    const int ns = (int)((kTcSmemCap - fixed) / g.stage_bytes) - nlo;
     g.nstage = ns < tc::MAX_STAGE ? ns : tc::MAX_STAGE;
     g.raw_pitch = raw_pitch;
-    g.smem_bytes = (uint32_t)(fixed + (size_t)g.nstage * g.stage_bytes);
+    g.smem_bytes = (uint32_t)(fixed + (size_t)(g.nstage + nlo) * g.stage_bytes);
     g.tmem_cols = 2 * tc::TMEM_BUF;
     return true;
 }
@@ -520,7 +627,7 @@ static cudaError_t launch_tc_cg(const ConvArgs &a, cudaStream_t st)
     constexpr int OROWB = CG * OSZ;
     tc::TcGeom g;
     const int groups = (a.Cout + CG - 1) / CG;
-    if (!tc_geometry(CG, NB, OP::KC, OP::ROWB * OP::SUB, groups, a.Cin, a.R * a.S, a.H, a.W, a.N, g))
+    if (!tc_geometry(CG, NB, OP::KC, OP::ROWB * OP::SUB, groups, a.Cin, a.R * a.S, a.H, a.W, a.N, OP::X3, g))
         return cudaErrorNotSupported;
     if ((long long)g.tiles_x * g.tiles_y * a.N > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     PFN_cuTensorMapEncodeTiled_v12000 encode = tc_tensor_map_encoder();
@@ -588,6 +695,11 @@ static cudaError_t launch_tc_groups(const ConvArgs &a, cudaStream_t st)
 }
 
 cudaError_t launch_conv_tc(const ConvArgs &a, cudaStream_t st) { return launch_tc_groups<tc::OpTF32, false>(a, st); }
+
+cudaError_t launch_conv_tc_x3(const ConvArgs &a, cudaStream_t st)
+{
+    return launch_tc_groups<tc::OpTF32x3, false>(a, st);
+}
 
 cudaError_t launch_conv_tc_bf16(const ConvArgs &a, bool y_bf16, cudaStream_t st)
 {

@@ -46,6 +46,9 @@ cudaError_t launch_conv_nhwc(const ConvArgs &a, cudaStream_t st);
 // Tensor-core (tcgen05) implicit-GEMM convolution, TF32 operands, NHWC, Cin % 4 == 0,
 // Cout <= 128, R, S <= 3 (conv_tc.cu).  cudaErrorNotSupported otherwise.
 cudaError_t launch_conv_tc(const ConvArgs &a, cudaStream_t st);
+// The same with split-TF32 operands (three MMAs per product, head and
+// correction accumulators; conv_tc.cu).
+cudaError_t launch_conv_tc_x3(const ConvArgs &a, cudaStream_t st);
 // BF16 operands (conv_tc.cu): a.x is a bf16 NHWC tensor, a.y bf16 (y_bf16)
 // or fp32; a.w, a.b fp32.
 cudaError_t launch_conv_tc_bf16(const ConvArgs &a, bool y_bf16, cudaStream_t st);

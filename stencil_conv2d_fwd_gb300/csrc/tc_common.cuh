@@ -32,14 +32,44 @@ constexpr int CH = 32;          // channels per stage (one swizzled row per pixe
 //    two sub-buffers of 32-byte rows (16 channels, one K step each).  The
 //    fp32 filters are rounded to bf16 (to nearest even) when the CTA stages
 //    them.
+//  * OpTF32x3: OpTF32's layout with every operand split into a TF32 head and
+//    a remainder, v = hi(v) + lo(v), hi(v) = v with its 13 low mantissa bits
+//    cleared (exactly a TF32 value), lo(v) = v - hi(v) (exact in fp32, at most
+//    2^-10 |v|).  Each product is x_hi w_hi + (x_hi w_lo + x_lo w_hi): the
+//    dropped x_lo w_lo is below 2^-20 |x w|, and the remainders lose at most
+//    2^-10 of themselves to the TF32 conversion, so every product is within
+//    ~3 * 2^-20 of exact ("split" or "3xTF32" tensor-core arithmetic, as in
+//    Ootomo and Yokota, "Recovering single precision accuracy from Tensor
+//    Cores while surpassing the FP32 theoretical peak performance", 2022).
+//    The head products and the two correction products go to separate
+//    accumulators, added once in the epilogue, so the small corrections are
+//    not rounded against the large running sum.  The filter bank stacks
+//    heads and remainders in N, so x_hi [w_hi | w_lo] is one MMA of twice
+//    the width (head and first correction side by side in tensor memory)
+//    and x_lo w_hi a second one into the correction columns.
 struct OpTF32 {
     static constexpr int ESZ = 4, KC = 8, ROWB = 128, SUB = 1;
     static constexpr uint32_t A_LAYOUT = 2, FMT = 2;   // descriptor layout 128B swizzle; TF32
+    static constexpr bool X3 = false;
 };
 struct OpBF16 {
     static constexpr int ESZ = 2, KC = 16, ROWB = 32, SUB = 2;
     static constexpr uint32_t A_LAYOUT = 6, FMT = 1;   // descriptor layout 32B swizzle; BF16
+    static constexpr bool X3 = false;
 };
+struct OpTF32x3 {
+    static constexpr int ESZ = 4, KC = 8, ROWB = 128, SUB = 1;
+    static constexpr uint32_t A_LAYOUT = 2, FMT = 2;
+    static constexpr bool X3 = true;
+};
+
+// The TF32 head of an fp32 value (13 low mantissa bits cleared) and the
+// remainder v - head, both as raw bits.
+__device__ __forceinline__ uint32_t tf32_head(uint32_t v) { return v & 0xFFFFE000u; }
+__device__ __forceinline__ uint32_t tf32_rest(uint32_t v)
+{
+    return __float_as_uint(__fsub_rn(__uint_as_float(v), __uint_as_float(tf32_head(v))));
+}
 
 // Instruction descriptor: D = F32, A = B = FMT (TF32 2, BF16 1), both
 // K-major, dense, M = 128.
@@ -179,11 +209,15 @@ __device__ __forceinline__ int stg_key(int p)
 // One unit is one output channel and one block of CU input channels (one
 // 16-byte chunk); neighbouring threads take neighbouring output channels,
 // whose B rows are neighbours.  Threads lt = 0 .. LT-1 share the work.
+// OP::X3: each (k, r, cb) block has 2 NB rows, the TF32 heads in rows
+// [0, NB) and the remainders in rows [NB, 2 NB), so that one MMA of
+// N = 2 NB multiplies A by both.
 template <int CG, class OP>
 __device__ __forceinline__ void stage_filter_bank(const float *raw, uint4 *bank, int raw_pitch, int co_n, int Cin, int R,
                                                   int S, int nk, int lt, int LT)
 {
     constexpr int NB = (3 * CG + 15) / 16 * 16;
+    constexpr int RB = OP::X3 ? 2 * NB : NB;   // rows per (k, r, cb) block
     constexpr int CU = OP::KC / 2;
     const int RS = R * S;
     const int units = CG * 2 * nk;
@@ -215,21 +249,28 @@ __device__ __forceinline__ void stage_filter_bank(const float *raw, uint4 *bank,
         for (int t = 0; t < 9; ++t) {
             const int r = t / 3, s = t % 3;
             uint4 o;
+            const int at = ((k * 3 + r) * 2 + cb) * RB + s * CG + co;
             if constexpr (CU == 4) {
                 o = make_uint4(__float_as_uint(f[t]), __float_as_uint(f[9 + t]), __float_as_uint(f[18 + t]),
                                __float_as_uint(f[27 + t]));
+                if constexpr (OP::X3) {
+                    bank[at + NB] = make_uint4(tf32_rest(o.x), tf32_rest(o.y), tf32_rest(o.z), tf32_rest(o.w));
+                    o = make_uint4(tf32_head(o.x), tf32_head(o.y), tf32_head(o.z), tf32_head(o.w));
+                }
             } else {
                 o = make_uint4(pack_bf16(f[t], f[9 + t]), pack_bf16(f[18 + t], f[27 + t]), pack_bf16(f[36 + t], f[45 + t]),
                                pack_bf16(f[54 + t], f[63 + t]));
             }
-            bank[((k * 3 + r) * 2 + cb) * NB + s * CG + co] = o;
+            bank[at] = o;
         }
     }
     // B rows n >= 3 * CG (N rounded up to a multiple of 16) are zero
     constexpr int PADN = NB - 3 * CG;
     if constexpr (PADN > 0) {
-        for (int e = lt; e < nk * 3 * 2 * PADN; e += LT)
-            bank[(e / PADN) * NB + 3 * CG + e % PADN] = make_uint4(0u, 0u, 0u, 0u);
+        for (int e = lt; e < nk * 3 * 2 * PADN; e += LT) {
+            bank[(e / PADN) * RB + 3 * CG + e % PADN] = make_uint4(0u, 0u, 0u, 0u);
+            if constexpr (OP::X3) bank[(e / PADN) * RB + NB + 3 * CG + e % PADN] = make_uint4(0u, 0u, 0u, 0u);
+        }
     }
 }
 
