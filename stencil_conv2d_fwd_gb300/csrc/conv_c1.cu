@@ -12,7 +12,12 @@
 //  * every thread of a warp reads the same filter tap at the same time, so
 //    filter reads are broadcasts (Section 3.2.2 puts them in constant
 //    memory; here the CTA stages them once in shared memory, which gives
-//    the same broadcast without a per-call constant-bank upload).
+//    the same broadcast without a per-call constant-bank upload; a
+//    constant-bank variant, one weight operand per FMA, measured 2x slower
+//    on GB300).
+// Groups of 32 output channels use a tiled form of the same sweep
+// (conv_c1_tile_kernel below): the band's input rows are staged in shared
+// memory once, and each thread computes 8 channels x 8 pixels.
 // The FMAs run as packed dual-FP32 FMAs (__ffma2_rn) on pairs of output
 // channels; each component rounds like fmaf.
 // Horizontal sharing between neighbouring threads goes through warp
@@ -295,22 +300,13 @@ __global__ void __launch_bounds__(256)
 // The accumulators start at the bias (the sum's first term instead of its
 // last; the rounding stays within the FP32 bound), read from shared memory
 // with the filters, and the stores need one in-image test per thread.
-// TMA_OUT (32 output channels per CTA): a warp writes its output row (32
-// pixels x 32 channels, 128-byte pixel rows with the 128-byte swizzle) into
-// one of its two shared-memory buffers and lane 0 stores it with one TMA
-// copy (pixels past W and channels past Cout clipped by the copy), so the
-// global stores leave the load/store unit's data pipe, which the filter
-// loads also use.
-template <int K, int F_T, int CL, bool TMA_OUT>
+template <int K, int F_T, int CL>
 __global__ void __launch_bounds__(256, (K >= 7 && F_T >= 8) ? 1 : 2)
     conv_c1_ring_kernel(const float *__restrict__ x, const float *__restrict__ w,
                         const float *__restrict__ bias, float *__restrict__ y, int N, int H, int W,
-                        int Cout, int R, int S, int act, int rows_per_cta, int col_tiles,
-                        const __grid_constant__ CUtensorMap tmy)
+                        int Cout, int R, int S, int act, int rows_per_cta, int col_tiles)
 {
     using C = C1Cfg<K, F_T, CL>;
-    static_assert(!TMA_OUT || (F_T == 8 && CL == 4), "TMA stores: 32 channels (128-byte pixel rows) per CTA");
-    extern __shared__ __align__(1024) unsigned char c1_out_raw[];
     __shared__ __align__(16) float ws[K * K * C::CO_CTA];
     __shared__ __align__(16) float bs[C::CO_CTA];
 
@@ -433,34 +429,7 @@ __global__ void __launch_bounds__(256, (K >= 7 && F_T >= 8) ? 1 : 2)
                 }
             }
             raw_c = raw_n;
-            if constexpr (TMA_OUT) {
-                // buffer i % 2 of this warp (1024-byte aligned, 4 KB)
-                const uint32_t raw_u = smem_u32(c1_out_raw);
-                const uint32_t buf = ((raw_u + 1023) & ~1023u) + (uint32_t)((warp * 2 + (i & 1)) * 4096);
-                const int xw = (ct * nwarps + warp) * (C::PL * 4);   // the warp's first pixel
-                if (lane == 0) bulk_wait_read<1>();   // the store that last read this buffer is done
-                __syncwarp();
-                if (px_ok) {
-#pragma unroll
-                    for (int g = 0; g < F_T / 4; ++g)
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int p = 4 * pl + j;          // pixel of the warp's row
-                            const int q = g * 4 + cl;          // 16-byte chunk: channels 4q .. 4q + 3
-                            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(
-                                             buf + p * 128 + ((q ^ (p & 7)) << 4)),
-                                         "f"(relu_if(acc[4 * g + 0][j], act)), "f"(relu_if(acc[4 * g + 1][j], act)),
-                                         "f"(relu_if(acc[4 * g + 2][j], act)), "f"(relu_if(acc[4 * g + 3][j], act))
-                                         : "memory");
-                        }
-                }
-                fence_proxy_async_smem();   // these writes -> visible to the copy
-                __syncwarp();
-                if (lane == 0 && xw < W) {
-                    tma_store_4d(&tmy, buf, co0, xw, oy, n);
-                    bulk_commit();
-                }
-            } else if (px_ok) {
+            if (px_ok) {
                 float *yrow = y + ((long long)n * H + oy) * W * Cout;
                 if constexpr (F_T >= 4) {
 #pragma unroll
@@ -488,43 +457,209 @@ __global__ void __launch_bounds__(256, (K >= 7 && F_T >= 8) ? 1 : 2)
             }
         }
     }
-    if constexpr (TMA_OUT)
-        if (lane == 0) bulk_wait_all();   // every store has written global memory
 }
 
 // The driver's tensor-map encoder (conv_tma_k3.cu), or nullptr.
 PFN_cuTensorMapEncodeTiled_v12000 conv_tma_encoder();
 
-// Output rows stored by TMA copies (32 channels per CTA, see the kernel).
-constexpr bool kC1TmaStores = true;
 
-template <int K, int F_T, int CL>
-static cudaError_t launch_c1_tma_out(const ConvArgs &a, cudaStream_t st, dim3 grid, int nwarps, int rows_per_cta,
-                                     int col_tiles)
+
+// Tiled variant for groups of 32 output channels (F_T = 8, CL = 4), W % 4
+// == 0 and 16-byte aligned x and y.  A CTA of four warps owns 256 image
+// columns and a band of rows; it stages the band's input rows (plus the
+// vertical halo) in shared memory once, then each thread computes 8 output
+// channels x 8 contiguous pixels of one row at a time (32 accumulator pairs),
+// reading the K rows of its window from the staged tile (four 16-byte loads
+// a row) instead of keeping a K-row ring in registers.  The FMA order is the
+// ring kernel's (bias first, then the taps row by row), so both give the
+// same bits.  Each warp stores its output row (64 pixels x 32 channels)
+// through a swizzled shared-memory buffer with one TMA copy; one buffer per
+// warp suffices (a row's arithmetic takes far longer than its copy's read of
+// the buffer), so four CTAs fit per SM.  Measured against the ring kernel
+// (1 -> 32, 5 x 5 on 1280 x 720): 38.6 -> 34.4 us; with two buffers and two
+// CTAs per SM 36.0 us, three CTAs 35.4 us.
+constexpr int kC1TileWarps = 4;
+constexpr int kC1TileCtas = 4;                 // resident CTAs per SM the grid is sized for
+constexpr int kC1TilePx = 64 * kC1TileWarps;   // tile columns
+constexpr int kC1TilePitch = kC1TilePx + 8;    // staged floats per row: image columns tx0 - 4 .. tx0 + 259
+constexpr int kC1TileOutBuf = 64 * 128;        // one output row of a warp: 64 pixels x 128 bytes
+
+template <int K>
+__global__ void __launch_bounds__(32 * kC1TileWarps, kC1TileCtas)
+    conv_c1_tile_kernel(const float *__restrict__ x, const float *__restrict__ w, const float *__restrict__ bias,
+                        int N, int H, int W, int Cout, int R, int S, int act, int rows_per_cta, int col_tiles,
+                        const __grid_constant__ CUtensorMap tmy)
+{
+    constexpr int HALO = K / 2;
+    constexpr int CO = 32;   // output channels per CTA
+    constexpr int PX = 8;    // pixels per thread
+    static_assert(HALO <= 4, "the staged row keeps 4 columns of halo room on each side");
+    extern __shared__ __align__(1024) unsigned char c1t_raw[];
+    __shared__ __align__(16) float ws[K * K * CO];
+    __shared__ __align__(16) float bs[CO];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cl = lane & 3, pl = lane >> 2;   // 4 channel lanes x 8 pixel lanes
+    const int co0 = blockIdx.y * CO;
+    const int n = blockIdx.z;
+    const int ct = blockIdx.x % col_tiles, rt = blockIdx.x / col_tiles;
+    const int tx0 = ct * kC1TilePx;
+    const int y0 = rt * rows_per_cta;
+    const int y1 = min(H, y0 + rows_per_cta);
+    const int nrows = y1 - y0, nin = nrows + K - 1;
+    // dynamic shared memory: [an output buffer per warp][input tile]
+    const uint32_t raw_u = smem_u32(c1t_raw);
+    const uint32_t obase = (raw_u + 1023) & ~1023u;
+    float *tile = reinterpret_cast<float *>(c1t_raw + (obase - raw_u) + kC1TileWarps * kC1TileOutBuf);
+
+    for (int e = tid; e < K * K * CO; e += 32 * kC1TileWarps) {
+        const int col = e % CO, tap = e / CO;
+        const int r = tap / K - (K - R) / 2, s = tap % K - (K - S) / 2;
+        const int co = co0 + col;
+        float v = 0.f;
+        if (r >= 0 && r < R && s >= 0 && s < S && co < Cout) v = w[((long long)co * R + r) * S + s];
+        ws[e] = v;
+    }
+    for (int e = tid; e < CO; e += 32 * kC1TileWarps) bs[e] = (bias && co0 + e < Cout) ? bias[co0 + e] : 0.f;
+    // staged column c of row r is image pixel (y0 - HALO + r, tx0 - 4 + c);
+    // 16-byte pieces are wholly inside or outside the image (W % 4 == 0)
+    // two copy groups: the K rows of the first output row, then the rest,
+    // which land while the first row is computed
+    const float *xn = x + (long long)n * H * W;
+    constexpr int CPR = kC1TilePitch / 4;
+    auto stage_rows = [&](int r0, int r1) {
+        for (int e = r0 * CPR + tid; e < r1 * CPR; e += 32 * kC1TileWarps) {
+            const int r = e / CPR, q = e % CPR;
+            const int iy = y0 - HALO + r, ix = tx0 - 4 + 4 * q;
+            const bool ok = iy >= 0 && iy < H && ix >= 0 && ix + 3 < W;
+            cp_async16(smem_u32(tile + r * kC1TilePitch + 4 * q), ok ? xn + (long long)iy * W + ix : x, ok ? 16 : 0);
+        }
+        cp_async_commit();
+    };
+    stage_rows(0, K);
+    stage_rows(K, nin);
+    cp_async_wait<1>();
+    __syncthreads();
+
+    const int xw = tx0 + warp * 64;             // the warp's first column
+    const int cb = warp * 64 + pl * PX;         // staged column of this thread's pixel x - 4
+    const uint32_t buf = obase + (uint32_t)(warp * kC1TileOutBuf);
+    for (int i = 0; i < nrows; ++i) {
+        const int oy = y0 + i;
+        if (i == 1) {   // the rest of the band has landed
+            cp_async_wait<0>();
+            __syncthreads();
+        }
+        float acc[8][PX];
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            const float4 b4 = *reinterpret_cast<const float4 *>(bs + g * 16 + 4 * cl);
+#pragma unroll
+            for (int j = 0; j < PX; ++j) {
+                acc[4 * g + 0][j] = b4.x;
+                acc[4 * g + 1][j] = b4.y;
+                acc[4 * g + 2][j] = b4.z;
+                acc[4 * g + 3][j] = b4.w;
+            }
+        }
+#pragma unroll
+        for (int ky = 0; ky < K; ++ky) {
+            // image columns x - 4 .. x + 11 of input row oy - HALO + ky
+            const float *trow = tile + (i + ky) * kC1TilePitch + cb;
+            float win[16];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 t = *reinterpret_cast<const float4 *>(trow + 4 * q);
+                win[4 * q] = t.x;
+                win[4 * q + 1] = t.y;
+                win[4 * q + 2] = t.z;
+                win[4 * q + 3] = t.w;
+            }
+#pragma unroll
+            for (int kx = 0; kx < K; ++kx) {
+                const float *wt = ws + (ky * K + kx) * CO;
+                float wv[8];
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    const float4 t = *reinterpret_cast<const float4 *>(wt + g * 16 + 4 * cl);
+                    wv[4 * g + 0] = t.x;
+                    wv[4 * g + 1] = t.y;
+                    wv[4 * g + 2] = t.z;
+                    wv[4 * g + 3] = t.w;
+                }
+#pragma unroll
+                for (int j = 0; j < PX; ++j) {
+                    const float v = win[4 - HALO + j + kx];
+                    const float2 vv = make_float2(v, v);
+#pragma unroll
+                    for (int f = 0; f < 8; f += 2) {
+                        float2 a2 = make_float2(acc[f][j], acc[f + 1][j]);
+                        a2 = __ffma2_rn(make_float2(wv[f], wv[f + 1]), vv, a2);
+                        acc[f][j] = a2.x;
+                        acc[f + 1][j] = a2.y;
+                    }
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_read<0>();   // the store that last read this buffer is done
+        __syncwarp();
+        if (xw < W) {
+#pragma unroll
+            for (int g = 0; g < 2; ++g)
+#pragma unroll
+                for (int j = 0; j < PX; ++j) {
+                    const int p = pl * PX + j;   // pixel of the warp's row
+                    const int q = g * 4 + cl;    // 16-byte chunk: channels 4q .. 4q + 3
+                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(buf + p * 128 + ((q ^ (p & 7)) << 4)),
+                                 "f"(relu_if(acc[4 * g + 0][j], act)), "f"(relu_if(acc[4 * g + 1][j], act)),
+                                 "f"(relu_if(acc[4 * g + 2][j], act)), "f"(relu_if(acc[4 * g + 3][j], act))
+                                 : "memory");
+                }
+        }
+        fence_proxy_async_smem();   // these writes -> visible to the copy
+        __syncwarp();
+        if (lane == 0 && xw < W) {
+            tma_store_4d(&tmy, buf, co0, xw, oy, n);
+            bulk_commit();
+        }
+    }
+    if (lane == 0) bulk_wait_all();   // every store has written global memory
+}
+
+template <int K>
+static cudaError_t launch_c1_tile(const ConvArgs &a, cudaStream_t st)
 {
     PFN_cuTensorMapEncodeTiled_v12000 encode = conv_tma_encoder();
     if (!encode) return cudaErrorNotSupported;
-    // NHWC output as (C, W, H, N); box = 32 channels x 32 pixels of one row
+    const int col_tiles = (a.W + kC1TilePx - 1) / kC1TilePx;
+    const int groups = (a.Cout + 31) / 32;
+    // one wave: bands of rows so that every CTA is resident at once
+    const long long per_band = (long long)col_tiles * groups * a.N;
+    long long bands = (long long)kC1TileCtas * device_sm_count() / per_band;
+    if (bands < 1) bands = 1;
+    int rows_per_cta = (int)((a.H + bands - 1) / bands);
+    if (rows_per_cta > 48) rows_per_cta = 48;   // bounds the staged tile
+    const long long nb = (long long)col_tiles * ((a.H + rows_per_cta - 1) / rows_per_cta);
+    if (nb > 0x7fffffffLL || groups > 65535 || a.N > 65535) return cudaErrorInvalidConfiguration;
     CUtensorMap tm;
     const cuuint64_t dims[4] = {(cuuint64_t)a.Cout, (cuuint64_t)a.W, (cuuint64_t)a.H, (cuuint64_t)a.N};
     const cuuint64_t strides[3] = {(cuuint64_t)a.Cout * 4, (cuuint64_t)a.W * a.Cout * 4,
                                    (cuuint64_t)a.H * a.W * a.Cout * 4};
-    const cuuint32_t box[4] = {32, 32, 1, 1};
+    const cuuint32_t box[4] = {32, 64, 1, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     if (encode(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.y, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorNotSupported;
-    const int smem = nwarps * 2 * 4096 + 1024;   // two 4 KB row buffers per warp + alignment slack
+    const int smem = kC1TileWarps * kC1TileOutBuf + 1024 + (rows_per_cta + K - 1) * kC1TilePitch * 4;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     static KernelCache cache;
-    e = ensure_dynamic_smem(cache, dev, conv_c1_ring_kernel<K, F_T, CL, true>, smem);
+    e = ensure_dynamic_smem(cache, dev, conv_c1_tile_kernel<K>, smem);
     if (e != cudaSuccess) return e;
-    conv_c1_ring_kernel<K, F_T, CL, true><<<grid, nwarps * 32, smem, st>>>(
-        a.x, a.w, a.b, a.y, a.N, a.H, a.W, a.Cout, a.R, a.S, a.act, rows_per_cta, col_tiles, tm);
+    conv_c1_tile_kernel<K><<<dim3((unsigned)nb, groups, a.N), 32 * kC1TileWarps, smem, st>>>(
+        a.x, a.w, a.b, a.N, a.H, a.W, a.Cout, a.R, a.S, a.act, rows_per_cta, col_tiles, tm);
     return cudaGetLastError();
 }
 
@@ -551,23 +686,22 @@ static cudaError_t launch_c1_cfg(const ConvArgs &a, cudaStream_t st)
     if (nb > 0x7fffffffLL || groups > 65535 || a.N > 65535) return cudaErrorInvalidConfiguration;
     const int vec = ((a.W & 3) == 0) && ((reinterpret_cast<uintptr_t>(a.x) & 15) == 0) &&
                     ((reinterpret_cast<uintptr_t>(a.y) & 15) == 0);
-    // the ring needs more registers than 7 x 7 filters with 8 channels per
-    // thread leave at 2 CTAs per SM; those keep the shifting window
-    if (vec && !(K >= 7 && F_T >= 8)) {
+    if (vec) {
+        // groups of 32 channels: the tiled kernel (any filter size up to 7)
         if constexpr (F_T == 8 && CL == 4) {
-            if (kC1TmaStores) {
-                const cudaError_t e = launch_c1_tma_out<K, F_T, CL>(a, st, dim3((unsigned)nb, groups, a.N), nwarps,
-                                                                    rows_per_cta, col_tiles);
-                if (e != cudaErrorNotSupported) return e;
-            }
+            const cudaError_t e = launch_c1_tile<K>(a, st);
+            if (e != cudaErrorNotSupported) return e;
         }
-        CUtensorMap unused;
-        std::memset(&unused, 0, sizeof(unused));
-        conv_c1_ring_kernel<K, F_T, CL, false><<<dim3((unsigned)nb, groups, a.N), nwarps * 32, 0, st>>>(
-            a.x, a.w, a.b, a.y, a.N, a.H, a.W, a.Cout, a.R, a.S, a.act, rows_per_cta, col_tiles, unused);
-    } else
-        conv_c1_kernel<K, F_T, CL><<<dim3((unsigned)nb, groups, a.N), nwarps * 32, 0, st>>>(
-            a.x, a.w, a.b, a.y, a.N, a.H, a.W, a.Cout, a.R, a.S, a.act, rows_per_cta, col_tiles, vec);
+        // the ring needs more registers than 7 x 7 filters with 8 channels
+        // per thread leave at 2 CTAs per SM; those keep the shifting window
+        if (!(K >= 7 && F_T >= 8)) {
+            conv_c1_ring_kernel<K, F_T, CL><<<dim3((unsigned)nb, groups, a.N), nwarps * 32, 0, st>>>(
+                a.x, a.w, a.b, a.y, a.N, a.H, a.W, a.Cout, a.R, a.S, a.act, rows_per_cta, col_tiles);
+            return cudaGetLastError();
+        }
+    }
+    conv_c1_kernel<K, F_T, CL><<<dim3((unsigned)nb, groups, a.N), nwarps * 32, 0, st>>>(
+        a.x, a.w, a.b, a.y, a.N, a.H, a.W, a.Cout, a.R, a.S, a.act, rows_per_cta, col_tiles, vec);
     return cudaGetLastError();
 }
 

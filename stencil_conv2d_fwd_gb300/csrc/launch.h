@@ -102,11 +102,12 @@ struct KernelCache {
 std::mutex &launch_cache_mutex();
 
 // Opts `kernel` in to `smem` bytes of dynamic shared memory on device dev
-// (0 <= dev < 64), once per size increase.
+// (0 <= dev < 64), once per size increase.  Also below 48 KB: without the
+// opt-in, static and dynamic shared memory together are capped at 48 KB.
 template <class K>
 cudaError_t ensure_dynamic_smem(KernelCache &c, int dev, K kernel, int smem)
 {
-    if (smem <= 48 * 1024 || c.allowed[dev].load(std::memory_order_acquire) >= smem) return cudaSuccess;
+    if (smem <= 0 || c.allowed[dev].load(std::memory_order_acquire) >= smem) return cudaSuccess;
     std::lock_guard<std::mutex> lock(launch_cache_mutex());
     if (c.allowed[dev].load(std::memory_order_relaxed) >= smem) return cudaSuccess;
     const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

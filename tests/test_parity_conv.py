@@ -108,6 +108,11 @@ C1_SHAPES = [
     # more than 16 channels, W % 4 == 0 (two output rows per pass): odd band
     # ends, channel groups past Cout, 3x3 and 5x5
     (1, 32, 13, 44, 3, 3), (2, 24, 9, 40, 5, 5), (1, 32, 7, 8, 5, 5), (1, 64, 11, 36, 3, 3),
+    # the tiled kernel (17-32 channels per group, W % 4 == 0): a tile past the
+    # image's right edge, channel groups past Cout, every filter size incl.
+    # 7 x 7 and non-square, one-row images, N > 1
+    (2, 32, 37, 300, 5, 5), (1, 40, 9, 516, 7, 7), (1, 32, 1, 4, 3, 3), (1, 36, 13, 260, 1, 1),
+    (1, 32, 11, 128, 3, 5), (3, 48, 5, 68, 5, 5),
 ]
 
 
