@@ -603,15 +603,22 @@ __global__ void __launch_bounds__(32 * kC1TileWarps, kC1TileCtas)
         if (lane == 0) bulk_wait_read<0>();   // the store that last read this buffer is done
         __syncwarp();
         if (xw < W) {
+            // lanes of odd pixel lanes write pixel j ^ 4 when the others
+            // write pixel j: the two pixel lanes of an 8-lane phase then
+            // land in different swizzle rows (no bank conflict)
+            const bool odd = pl & 1;
 #pragma unroll
             for (int g = 0; g < 2; ++g)
 #pragma unroll
                 for (int j = 0; j < PX; ++j) {
-                    const int p = pl * PX + j;   // pixel of the warp's row
-                    const int q = g * 4 + cl;    // 16-byte chunk: channels 4q .. 4q + 3
+                    const int jj = odd ? (j ^ 4) : j;
+                    const int p = pl * PX + jj;   // pixel of the warp's row
+                    const int q = g * 4 + cl;     // 16-byte chunk: channels 4q .. 4q + 3
+                    float o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[e] = relu_if(odd ? acc[4 * g + e][j ^ 4] : acc[4 * g + e][j], act);
                     asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(buf + p * 128 + ((q ^ (p & 7)) << 4)),
-                                 "f"(relu_if(acc[4 * g + 0][j], act)), "f"(relu_if(acc[4 * g + 1][j], act)),
-                                 "f"(relu_if(acc[4 * g + 2][j], act)), "f"(relu_if(acc[4 * g + 3][j], act))
+                                 "f"(o[0]), "f"(o[1]), "f"(o[2]), "f"(o[3])
                                  : "memory");
                 }
         }
