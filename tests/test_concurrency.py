@@ -38,6 +38,8 @@ CASES = [
     ("nchw workspace", 2, 16, 24, 9, 40, 3, sc.SC_NCHW, "fp32"),
     ("cp.async 5x5", 1, 16, 8, 11, 30, 5, sc.SC_NHWC, "fp32"),
     ("tensor core", 1, 32, 32, 10, 40, 3, sc.SC_NHWC, "tc"),
+    ("tensor core split", 1, 32, 32, 10, 40, 3, sc.SC_NHWC, "x3"),
+    ("one channel tiled", 1, 1, 32, 9, 300, 5, sc.SC_NHWC, "fp32"),
 ]
 gate = threading.Barrier(len(CASES) + 1)
 errors = []
@@ -57,6 +59,8 @@ def run_conv(k, name, N, Cin, Cout, H, W, R, layout, entry):
         for _ in range(4):
             if entry == "tc":
                 rc = sc.conv2d_fwd_tc(xd, wd, bd, yd, N, H, W, Cin, Cout, R, R, L.act, stream=s)
+            elif entry == "x3":
+                rc = sc.conv2d_fwd_tc_x3(xd, wd, bd, yd, N, H, W, Cin, Cout, R, R, L.act, stream=s)
             else:
                 rc = sc.conv2d_fwd(xd, wd, bd, yd, N, H, W, Cin, Cout, R, R, layout, L.act, stream=s)
             if rc != 0:

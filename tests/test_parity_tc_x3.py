@@ -96,6 +96,14 @@ def test_x3_same_sign_sums(oracle_mod, cuda_dev, sc):
     assert_conv_close(y, yr, a, what="tc_x3 same-sign")
 
 
+def test_x3_without_bias_and_several_images(oracle_mod, cuda_dev, sc):
+    c = S.conv_case(933, 3, 24, 28, 11, 47, 3, 3, act=1)
+    L = c.layers[0]
+    y = conv_tc(sc.conv2d_fwd_tc_x3, c.x, L.w, None, L.act, cuda_dev)
+    yr, a = oracle_mod.conv2d_nchw(c.x, L.w, np.zeros(L.cout, dtype=np.float32), L.act)
+    assert_conv_close(y, yr, a, what="tc_x3 no bias")
+
+
 def test_x3_rejects_what_it_does_not_run(cuda_dev, sc):
     x = torch.zeros(4 * 8 * 8 * 6, device=cuda_dev)
     w = torch.zeros(4 * 6 * 25, device=cuda_dev)
