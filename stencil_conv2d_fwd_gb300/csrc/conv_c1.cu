@@ -476,8 +476,9 @@ PFN_cuTensorMapEncodeTiled_v12000 conv_tma_encoder();
 // through a swizzled shared-memory buffer with one TMA copy; one buffer per
 // warp suffices (a row's arithmetic takes far longer than its copy's read of
 // the buffer), so four CTAs fit per SM.  Measured against the ring kernel
-// (1 -> 32, 5 x 5 on 1280 x 720): 38.6 -> 34.4 us; with two buffers and two
-// CTAs per SM 36.0 us, three CTAs 35.4 us.
+// (1 -> 32, 5 x 5 on 1280 x 720): 38.6 -> 34.4 us (33.4 us with the
+// staggered buffer writes below); with two buffers and two CTAs per SM
+// 36.0 us, three CTAs 35.4 us.
 constexpr int kC1TileWarps = 4;
 constexpr int kC1TileCtas = 4;                 // resident CTAs per SM the grid is sized for
 constexpr int kC1TilePx = 64 * kC1TileWarps;   // tile columns
