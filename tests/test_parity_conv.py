@@ -12,7 +12,7 @@ import torch
 
 import synthetic as S
 import stencil_conv2d_fwd_gb300 as sc
-from parity_util import assert_conv_close, conv_gpu
+from parity_util import assert_conv_close, conv_gpu, nchw_to_nhwc, nhwc_to_nchw
 
 pytestmark = pytest.mark.gpu
 
@@ -51,6 +51,39 @@ def test_upscaling_net_layer_by_layer_and_end_to_end(oracle_mod, cuda_dev, sc):
         prop = torch.nn.functional.conv2d(torch.from_numpy(Ein), torch.from_numpy(np.abs(L.w).astype(np.float64)),
                                           padding=(L.r // 2, L.s // 2)).numpy()
         E = 1e-5 * a + prop   # a: scale of this layer at the GPU's own input
+        x, x64 = y, y64
+    err = np.abs(x.astype(np.float64) - x64)
+    assert (err <= E).all(), f"end-to-end error {err.max()} exceeds the propagated bound"
+
+
+def test_upscaling_net_with_split_tf32_layer_end_to_end(oracle_mod, cuda_dev, sc):
+    """The net with its 32 -> 32 layer on conv2d_fwd_tc_x3 (the other layers on
+    conv2d_fwd): each layer within 1e-5 * A of the oracle fed the GPU's own
+    input, and the final output within the bound propagated through the
+    all-fp64 chain, as for the FFMA net above."""
+    c = S.config(3)
+    x = c.x
+    x64 = c.x.astype(np.float64)
+    E = np.zeros_like(x64)
+    u = 2.0 ** -24
+    for li, L in enumerate(c.layers):
+        if li == 1:
+            N, Cin, H, W = x.shape
+            xd = torch.from_numpy(nchw_to_nhwc(x)).to(cuda_dev)
+            wd, bd = torch.from_numpy(L.w).to(cuda_dev), torch.from_numpy(L.b).to(cuda_dev)
+            yd = torch.empty(N * H * W * L.cout, device=cuda_dev)
+            sc.check(sc.conv2d_fwd_tc_x3(xd, wd, bd, yd, N, H, W, Cin, L.cout, L.r, L.s, L.act), "conv2d_fwd_tc_x3")
+            torch.cuda.synchronize()
+            y = nhwc_to_nchw(yd.cpu().numpy().reshape(N, H, W, L.cout))
+        else:
+            y = conv_gpu(x, L.w, L.b, L.act, cuda_dev)
+        yr, a = oracle_mod.conv2d_nchw(x, L.w, L.b, L.act)
+        assert_conv_close(y, yr, a, what=f"layer {li + 1}")
+        y64, a64 = oracle_mod.conv2d_nchw(x64.astype(np.float32), L.w, L.b, L.act)
+        Ein = E + u * np.abs(x64) + np.abs(x64 - x64.astype(np.float32).astype(np.float64))
+        prop = torch.nn.functional.conv2d(torch.from_numpy(Ein), torch.from_numpy(np.abs(L.w).astype(np.float64)),
+                                          padding=(L.r // 2, L.s // 2)).numpy()
+        E = 1e-5 * a + prop
         x, x64 = y, y64
     err = np.abs(x.astype(np.float64) - x64)
     assert (err <= E).all(), f"end-to-end error {err.max()} exceeds the propagated bound"
