@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
     const int ns = g.nstage;
     // stage buffers need 1024-byte alignment (the 128-byte swizzle pattern)
     unsigned char *smem_raw = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
-    unsigned char *abuf = smem_raw;                      // ns activation stages (X3: their TF32 heads)
+    unsigned char *abuf = smem_raw;                      // ns activation stages (X3: read as their TF32 heads)
     // X3: X3_LO buffers for the remainders, same layout as a stage; stage j
     // (head buffer j % ns) puts its remainders in buffer j % X3_LO
     unsigned char *alo = abuf + (size_t)ns * g.stage_bytes;
@@ -360,10 +360,13 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
         }
     } else if (X3 && warp >= 6) {
         // ---------------------------------------------------- X3: converters
-        // Warps 6-9 split each landed stage in place: the TF32 heads over the
-        // copied values, the remainders into the stage's twin buffer (the
-        // same offsets, so the same swizzle phase); then the writes are made
-        // visible to the tensor core and the stage goes to the MMA warp.
+        // Warps 6-9 write each landed stage's remainders into a remainder
+        // buffer (the same offsets, so the same swizzle phase), make the
+        // writes visible to the tensor core and pass the stage to the MMA
+        // warp.  The heads need no pass: the TF32 MMA drops an fp32
+        // operand's 13 low mantissa bits (truncation, measured on sm_103a
+        // and pinned by tests/test_parity_tc.py), so it reads the copied
+        // values as exactly their heads.
         const int ct = tid - 6 * 32;
         const uint32_t nchunk = g.stage_bytes >> 4;
         constexpr int CB = 4;   // 16-byte chunks a thread loads before it writes
@@ -391,12 +394,9 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
 #pragma unroll
                 for (int q = 0; q < CB; ++q) {
                     const uint32_t c = c0 + 128 * q;
-                    if (c < nchunk) {
+                    if (c < nchunk)
                         lp[c] = make_uint4(tc::tf32_rest(v[q].x), tc::tf32_rest(v[q].y), tc::tf32_rest(v[q].z),
                                            tc::tf32_rest(v[q].w));
-                        hp[c] = make_uint4(tc::tf32_head(v[q].x), tc::tf32_head(v[q].y), tc::tf32_head(v[q].z),
-                                           tc::tf32_head(v[q].w));
-                    }
                 }
             }
             fence_proxy_async_smem();   // these writes -> visible to the tensor core

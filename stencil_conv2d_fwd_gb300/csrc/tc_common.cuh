@@ -46,7 +46,10 @@ constexpr int CH = 32;          // channels per stage (one swizzled row per pixe
 //    not rounded against the large running sum.  The filter bank stacks
 //    heads and remainders in N, so x_hi [w_hi | w_lo] is one MMA of twice
 //    the width (head and first correction side by side in tensor memory)
-//    and x_lo w_hi a second one into the correction columns.
+//    and x_lo w_hi a second one into the correction columns.  The MMA
+//    itself drops an fp32 operand's 13 low mantissa bits (truncation), so
+//    the activations' heads are the copied values as they are; only their
+//    remainders are written.
 struct OpTF32 {
     static constexpr int ESZ = 4, KC = 8, ROWB = 128, SUB = 1;
     static constexpr uint32_t A_LAYOUT = 2, FMT = 2;   // descriptor layout 128B swizzle; TF32

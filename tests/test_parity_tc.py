@@ -82,3 +82,29 @@ def test_tc_rejects_what_it_does_not_run(cuda_dev, sc):
     assert sc.conv2d_fwd_tc(x, wu, None, y, 1, 8, 8, 4, 4, 3, 3, 0) == sc.SC_ERR_ALIGN
     torch.cuda.synchronize()
     assert sc.sc_last_device_status() == sc.SC_OK
+
+
+def test_tf32_operands_are_truncated(cuda_dev, sc):
+    """The TF32 MMA reads an fp32 operand as its upper 19 bits (the 13 low
+    mantissa bits dropped, rounding toward zero).  conv2d_fwd_tc_x3 relies on
+    this: it feeds the copied activations to the MMA as their TF32 heads.  A
+    1 x 1 convolution with a unit weight (or a unit input) returns each
+    operand as the MMA saw it."""
+    vals = np.array([1 + 2 ** -11 + 2 ** -12, 1 + 2 ** -11, 1 + 2 ** -12, 1 + 2 ** -10 + 2 ** -11,
+                     -(1 + 2 ** -11 + 2 ** -12), 1 + 2 ** -11 + 2 ** -23, 3.0e-5 * (1 + 2 ** -11)], dtype=np.float32)
+    head = (vals.view(np.uint32) & np.uint32(0xFFFFE000)).view(np.float32)
+    n = len(vals)
+    for side in ("x", "w"):
+        got = []
+        for v in vals:
+            x = np.zeros((1, 1, 32, 4), np.float32)
+            w = np.zeros((4, 4, 1, 1), np.float32)
+            x[0, 0, 0, 0] = v if side == "x" else 1.0
+            w[0, 0, 0, 0] = 1.0 if side == "x" else v
+            yd = torch.zeros(32 * 4, device=cuda_dev)
+            sc.check(sc.conv2d_fwd_tc(torch.from_numpy(x).to(cuda_dev), torch.from_numpy(w).to(cuda_dev), None, yd,
+                                      1, 1, 32, 4, 4, 1, 1, 0), "conv2d_fwd_tc")
+            torch.cuda.synchronize()
+            got.append(yd.cpu().numpy()[0])
+        assert np.array_equal(np.array(got, np.float32), head), (side, got, head)
+    assert n == len(head)
