@@ -83,9 +83,11 @@ int conv2d_fwd(const float *x, const float *w, const float *b, float *y,
  * (pixels x output channels x (taps, input channels); "Optimizing Memory
  * Efficiency for Convolution Kernels on Kepler GPUs", Section 3.3, sets
  * this GEMM formulation against direct convolution).  x and w enter the
- * MMA as TF32 (10 explicit mantissa bits), products accumulate in fp32, so
- * results differ from conv2d_fwd by up to about 5e-3 * sum|x * w| per
- * element: a separate variant with its own tolerance, not a replacement.
+ * MMA as TF32 (10 explicit mantissa bits; the MMA drops the 13 low bits of
+ * an fp32 operand, a relative error below 2^-10 per operand), products
+ * accumulate in fp32, so results differ from conv2d_fwd by up to about
+ * 5e-3 * sum|x * w| per element: a separate variant with its own
+ * tolerance, not a replacement.
  * x, y : NHWC, 16-byte aligned.  w : OIHW, 16-byte aligned.  b : Cout
  *   floats or NULL.
  * Supported: Cin % 4 == 0, Cout % 4 == 0, Cout <= 128, R and S odd and <= 3,

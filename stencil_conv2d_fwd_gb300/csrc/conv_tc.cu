@@ -2,8 +2,8 @@
 // generation tensor cores (tcgen05, accumulators in tensor memory), TF32
 // operands, fp32 accumulation.  It computes the same operation as
 // conv2d_fwd (stride 1, zero "same" padding, bias, ReLU; R, S in {1, 3}) with
-// TF32 rounding of x and w, so it is checked with its own tolerance
-// (5e-3 * sum|x*w|).
+// x and w truncated to TF32 by the MMA, so it is checked with its own
+// tolerance (5e-3 * sum|x*w|).
 //
 // GEMM view ("Optimizing Memory Efficiency for Convolution Kernels on Kepler
 // GPUs", Section 3.3, compares direct convolution with the GEMM
