@@ -85,7 +85,7 @@ constexpr int X3_LO = 2;                     // split TF32: buffers for the stag
 constexpr int X3_STG_BYTES = 4 * OUT_BUF;    // split TF32: four epilogue warps
 
 struct TcGeom {
-    int MT, TR, THh;                // M-tiles per tile, tile rows (4 * MT), staged rows (TR + 2)
+    int MT, TR, THh;                // M-tiles per tile, tile rows (4 MT; RSN 4 MT - 2), staged rows (TR + 2)
     int tiles_x, tiles_y, ntiles;   // tiles of TC x TR output pixels, per image and in all
     int nk, nstg, nstage;           // K steps, 32-channel stages per tile, stage buffers
     int raw_pitch;                  // 16-byte units per output channel of the staged OIHW filters
@@ -97,15 +97,23 @@ struct TcGeom {
 __device__ __forceinline__ void give_up_flag(int &flag) { atomicExch(&flag, 1); }
 
 // CG: output channels per CTA (4, 8, 16 or 32); NB = MMA N = 3 * CG rounded
-// up to 16.  OP: operand kind (tc::OpTF32, tc::OpBF16).  YBF16: y is bf16
-// (else fp32).
-template <int CG, class OP, bool YBF16>
+// up to 16.  OP: operand kind (tc::OpTF32, tc::OpTF32x3, tc::OpBF16).
+// YBF16: y is bf16 (else fp32).  RSN (CG = 4, 3 x 3 filters): all nine taps
+// stacked in N (NB = 48), one MMA per K step and M-tile, the M rows being
+// the tile's staged rows (4 MT of them for 4 MT - 2 output rows); the
+// horizontal shifts are lane shuffles and the vertical ones, which cross
+// warps, are summed through shared memory in the epilogue.  With 4 output
+// channels the per-tap MMAs of N = 16 sit at the tensor core's fixed cost
+// per instruction; stacking the taps issues a third as many.
+template <int CG, class OP, bool YBF16, bool RSN = false>
 __global__ void __launch_bounds__(tc::NTHREADS, 1)
     conv_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmy,
                    const float *__restrict__ w, const float *__restrict__ bias, void *__restrict__ yv, int H, int W,
                    int Cin, int Cout, int R, int S, int act, tc::TcGeom g, int *status, unsigned long long timeout_ns)
 {
-    constexpr int NB = (3 * CG + 15) / 16 * 16;
+    static_assert(!RSN || CG == 4, "nine taps in N for 4-channel groups");
+    constexpr int NB = RSN ? (9 * CG + 15) / 16 * 16 : (3 * CG + 15) / 16 * 16;
+    constexpr int NR = RSN ? 1 : 3;                // vertical taps issued as A row offsets
     constexpr int KS = tc::CH / OP::KC;            // K steps per stage
     constexpr int KSUB = KS / OP::SUB;             // K steps per sub-buffer
     constexpr int CU = OP::KC / 2;                 // input channels per 16-byte B chunk
@@ -121,6 +129,7 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
     __shared__ __align__(8) unsigned long long full_bar[tc::MAX_STAGE], empty_bar[tc::MAX_STAGE];
     __shared__ __align__(8) unsigned long long conv_bar[X3 ? tc::MAX_STAGE : 1];   // X3: a stage is split
     __shared__ __align__(8) unsigned long long lo_empty[X3 ? tc::X3_LO : 1];       // X3: a remainder buffer is free
+    __shared__ __align__(8) unsigned long long rs_bar[RSN ? 2 : 1];                // RSN: a tile's row partial sums are in place
     __shared__ __align__(8) unsigned long long acc_full[2], acc_empty[2], w_bar, wt_bar;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
@@ -137,6 +146,7 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
     unsigned char *alo = abuf + (size_t)ns * g.stage_bytes;
     unsigned char *wsm = alo + (X3 ? (size_t)tc::X3_LO * g.stage_bytes : 0);   // resident filters (X3: heads and remainders)
     unsigned char *stg = wsm + g.w_bytes;                // epilogue transpose buffers
+    float *rsum = reinterpret_cast<float *>(stg);         // RSN: [2 tiles][3 taps r][TR rows][32 px][CG]
 
     // Filters, once per CTA.  The producer warp bulk-copies the group's OIHW
     // weights (one contiguous run of Cin * R * S floats per output channel)
@@ -169,6 +179,7 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
         for (int j = 0; j < 2; ++j) {
             mbar_init(smem_u32(&acc_full[j]), 1);
             mbar_init(smem_u32(&acc_empty[j]), X3 ? 4 : 8);   // one arrive per epilogue warp
+            if constexpr (RSN) mbar_init(smem_u32(&rs_bar[j]), X3 ? 4 : 8);
         }
         mbar_init(smem_u32(&w_bar), 1);
         mbar_init(smem_u32(&wt_bar), tc::NTHREADS / 32 - 1);   // every warp but the producer
@@ -190,9 +201,15 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
         const bool landed = mbar_wait_bounded(smem_u32(&w_bar), 0, timeout_ns);
         if (!landed) give_up_flag(abort_sh);
         constexpr int LT = tc::NTHREADS - 32;   // threads of every warp but the producer
-        if (landed)
-            tc::stage_filter_bank<CG, OP>(reinterpret_cast<const float *>(raw_sm), reinterpret_cast<uint4 *>(wsm),
-                                          g.raw_pitch, co_n, Cin, R, S, g.nk, warp < 4 ? tid : tid - 32, LT);
+        if (landed) {
+            if constexpr (RSN)
+                tc::stage_filter_bank_taps_in_n<CG, OP>(reinterpret_cast<const float *>(raw_sm),
+                                                        reinterpret_cast<uint4 *>(wsm), g.raw_pitch, co_n, Cin, g.nk,
+                                                        warp < 4 ? tid : tid - 32, LT);
+            else
+                tc::stage_filter_bank<CG, OP>(reinterpret_cast<const float *>(raw_sm), reinterpret_cast<uint4 *>(wsm),
+                                              g.raw_pitch, co_n, Cin, R, S, g.nk, warp < 4 ? tid : tid - 32, LT);
+        }
         // the staged weights' buffers go to the TMA (async proxy) next, the
         // bank to the tensor core
         fence_proxy_async_smem();
@@ -286,21 +303,21 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
 #pragma unroll
                     for (int kk = 0; kk < KS; ++kk)
 #pragma unroll
-                        for (int r = 0; r < 3; ++r)
+                        for (int r = 0; r < NR; ++r)
 #pragma unroll
                             for (int gi = 0; gi < G; ++gi)
                                 mma1(d0 + (uint32_t)(gi * DSTR), a0 + (uint32_t)(kk / KSUB) * asub + (uint32_t)((kk % KSUB) * 2 + r * AR + gi * AM),
-                                     b0 + (uint32_t)((kk * 3 + r) * 2 * RB), (kk > 0 || r > 0) ? 1u : acc0);
+                                     b0 + (uint32_t)((kk * NR + r) * 2 * RB), (kk > 0 || r > 0) ? 1u : acc0);
                     return;
                 }
 #pragma unroll 1
                 for (int kk = 0; kk < nks; ++kk) {
 #pragma unroll
-                    for (int r = 0; r < 3; ++r)
+                    for (int r = 0; r < NR; ++r)
 #pragma unroll
                         for (int gi = 0; gi < G; ++gi)
                             mma1(d0 + (uint32_t)(gi * DSTR), a0 + (uint32_t)(kk / KSUB) * asub + (uint32_t)((kk % KSUB) * 2 + r * AR + gi * AM),
-                                 b0 + (uint32_t)((kk * 3 + r) * 2 * RB), (kk > 0 || r > 0) ? 1u : acc0);
+                                 b0 + (uint32_t)((kk * NR + r) * 2 * RB), (kk > 0 || r > 0) ? 1u : acc0);
                 }
             };
             int s = 0, j = 0, committed = -1;
@@ -325,7 +342,7 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
                     const uint32_t a_lo = (a_base + (uint32_t)s * (g.stage_bytes >> 4)) | a_lbo;
                     if constexpr (X3)
                         alo_off = (uint32_t)(((size_t)(ns - s + j % tc::X3_LO) * g.stage_bytes) >> 4);
-                    const uint32_t b_lo = (w_base + (uint32_t)(c * KS * 3 * 2 * RB)) | b_lbo;
+                    const uint32_t b_lo = (w_base + (uint32_t)(c * KS * NR * 2 * RB)) | b_lbo;
                     const int nks = g.nk - KS * c < KS ? g.nk - KS * c : KS;
                     const uint32_t acc0 = c > 0 ? 1u : 0u;
                     int mt = 0;
@@ -439,6 +456,89 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
             int n, y0, x0;
             tile_origin(u, n, y0, x0);
             const uint32_t tbuf = tmem + (uint32_t)(b * tc::TMEM_BUF) + ((uint32_t)(q4 * 32) << 16);
+            if constexpr (RSN) {
+                // Staged row ty = 4 mt + q4 of this warp holds, per tap (r, s),
+                // the products for output row ty - r at column lane - s.  Per
+                // r, the lane-shifted sum over s goes to rsum[r][ty - r]; once
+                // every epilogue warp's sums are in place (a bounded mbarrier
+                // wait: a warp that gave up must not hold the others), each
+                // warp adds the three r for its output rows.  rsum holds two
+                // tiles, alternating, so tile u's writes never meet tile u - 1's
+                // reads (a warp writes tile u only after every warp arrived
+                // for tile u - 1, i.e. finished reading tile u - 2).
+                float *rb = rsum + (size_t)(u & 1) * (3 * g.TR * 32 * CG);
+                for (int mt = set; mt < g.MT; mt += MSTEP) {
+                    uint32_t rv[9][CG];
+#pragma unroll
+                    for (int t = 0; t < 9; ++t) tc::tmem_ld<CG>(tbuf + (uint32_t)(mt * DSTR + t * CG), rv[t]);
+                    tc::tmem_wait_ld();
+                    if constexpr (X3) {
+                        uint32_t cv[9][CG];
+#pragma unroll
+                        for (int t = 0; t < 9; ++t) tc::tmem_ld<CG>(tbuf + (uint32_t)(mt * DSTR + NB + t * CG), cv[t]);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int t = 0; t < 9; ++t)
+#pragma unroll
+                            for (int i = 0; i < CG; ++i)
+                                rv[t][i] = __float_as_uint(__uint_as_float(rv[t][i]) + __uint_as_float(cv[t][i]));
+                    }
+                    const int ty = mt * 4 + q4;
+#pragma unroll
+                    for (int r = 0; r < 3; ++r) {
+                        float c[CG];
+#pragma unroll
+                        for (int i = 0; i < CG; ++i)
+                            c[i] = __uint_as_float(rv[3 * r][i]) +
+                                   __shfl_down_sync(0xffffffffu, __uint_as_float(rv[3 * r + 1][i]), 1) +
+                                   __shfl_down_sync(0xffffffffu, __uint_as_float(rv[3 * r + 2][i]), 2);
+                        const int e = ty - r;
+                        if (e >= 0 && e < g.TR)
+                            *reinterpret_cast<float4 *>(rb + ((r * g.TR + e) * 32 + lane) * CG) =
+                                make_float4(c[0], c[1], c[2], c[3]);
+                    }
+                }
+                // every column this warp needs has been read: release the buffer
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&acc_empty[b]));
+                if (lane == 0) mbar_arrive(smem_u32(&rs_bar[u & 1]));
+                const bool all = mbar_wait_bounded(smem_u32(&rs_bar[u & 1]), (uint32_t)((u >> 1) & 1), timeout_ns);
+                if (__any_sync(0xffffffffu, !all)) {
+                    if (lane == 0) give_up();
+                    break;
+                }
+                constexpr int NEW = X3 ? 4 : 8;                   // epilogue warps
+                const int ew = warp < 4 ? warp : warp - 2;        // 0 .. NEW - 1
+                for (int e = ew; e < g.TR; e += NEW) {
+                    const int oy = y0 + e, ox = x0 + lane;
+                    if (lane < tc::TC && oy < H && ox < W) {
+                        float o[CG];
+#pragma unroll
+                        for (int i = 0; i < CG; ++i) o[i] = 0.f;
+#pragma unroll
+                        for (int r = 0; r < 3; ++r) {
+                            const float4 p = *reinterpret_cast<const float4 *>(rb + ((r * g.TR + e) * 32 + lane) * CG);
+                            o[0] += p.x;
+                            o[1] += p.y;
+                            o[2] += p.z;
+                            o[3] += p.w;
+                        }
+#pragma unroll
+                        for (int i = 0; i < CG; ++i) o[i] = relu_if(o[i] + bias_r[i], act);
+                        unsigned char *yp = reinterpret_cast<unsigned char *>(yv) +
+                                            ((((long long)n * H + oy) * W + ox) * Cout + co0) * OSZ;
+                        if (co0 < Cout) {
+                            if constexpr (YBF16)
+                                *reinterpret_cast<uint2 *>(yp) =
+                                    make_uint2(tc::pack_bf16(o[0], o[1]), tc::pack_bf16(o[2], o[3]));
+                            else
+                                *reinterpret_cast<float4 *>(yp) = make_float4(o[0], o[1], o[2], o[3]);
+                        }
+                    }
+                }
+                continue;
+            }
             const int last_mt = X3 ? g.MT - 1 : set + ((g.MT - 1 - set) & ~1);   // this set's last M-tile (< set: none)
             if (last_mt < set) {
                 // nothing of this tile for this warp: release the buffer at once
@@ -551,14 +651,26 @@ constexpr size_t kTcSmemCap = 227 * 1024 - 1024;
 // (twice the rows), an M-tile takes 2 * NB accumulator columns (heads and
 // corrections), and four epilogue warps need four output buffers.
 static bool tc_geometry(int Cg, int NB, int kc, int rowb, int groups, int Cin, int RS, int H, int W, int Nimg,
-                        bool x3, tc::TcGeom &g)
+                        bool x3, bool rsn, tc::TcGeom &g)
 {
     const int nk = (Cin + kc - 1) / kc;
-    const size_t w_bytes = ((size_t)nk * 3 * 2 * (x3 ? 2 * NB : NB) * 16 + 1023) & ~(size_t)1023;
+    // filter bank: (K step, [tap r,] 4-channel block) blocks of NB rows (x3: 2 NB)
+    const size_t w_bytes = ((size_t)nk * (rsn ? 1 : 3) * 2 * (x3 ? 2 * NB : NB) * 16 + 1023) & ~(size_t)1023;
     const int cols = x3 ? 2 * NB : NB;   // accumulator columns per M-tile
     const int nlo = x3 ? tc::X3_LO : 0;  // remainder buffers, each the size of a stage
-    const size_t fixed = w_bytes + (x3 ? tc::X3_STG_BYTES : tc::STG_BYTES) + 1024;   // + alignment slack
-    if (fixed >= kTcSmemCap) return false;
+    const size_t stg_base = x3 ? tc::X3_STG_BYTES : tc::STG_BYTES;
+    // rsn: output rows per tile = staged rows - 2 (the M rows are the staged
+    // rows), and the epilogue's row partial sums for two tiles share the
+    // output-buffer region
+    auto rows_out = [&](int MT) { return rsn ? 4 * MT - 2 : 4 * MT; };
+    auto rows_staged = [&](int MT) { return rsn ? 4 * MT : 4 * MT + 2; };
+    auto fixed_of = [&](int MT) {
+        size_t stg = stg_base;
+        const size_t rs = rsn ? (size_t)2 * 3 * rows_out(MT) * tc::WP * Cg * 4 : 0;
+        if (rs > stg) stg = rs;
+        return w_bytes + stg + 1024;   // + alignment slack
+    };
+    if (fixed_of(1) >= kTcSmemCap) return false;
     const int sms = device_sm_count() / groups > 0 ? device_sm_count() / groups : 1;   // CTAs per channel group
     const int tiles_x = (W + tc::TC - 1) / tc::TC;
     int best_mt = 0;
@@ -568,8 +680,9 @@ static bool tc_geometry(int Cg, int NB, int kc, int rowb, int groups, int Cin, i
     const int raw_pitch = tc::filter_raw_pitch(Cin, RS);
     const size_t raw = (size_t)Cg * raw_pitch * 16;
     for (int MT = 1; MT * cols <= tc::TMEM_BUF && MT <= 16; ++MT) {
-        const int TR = 4 * MT;
-        const size_t stage = (size_t)(TR + 2) * tc::WP * rowb;
+        const int TR = rows_out(MT);
+        const size_t stage = (size_t)rows_staged(MT) * tc::WP * rowb;
+        const size_t fixed = fixed_of(MT);
         if (fixed + (tc::MIN_STAGE + nlo) * stage > kTcSmemCap) break;
         const size_t nfit = (kTcSmemCap - fixed) / stage - nlo;
         if ((nfit < tc::MAX_STAGE ? nfit : tc::MAX_STAGE) * stage < raw) continue;
@@ -577,7 +690,7 @@ static bool tc_geometry(int Cg, int NB, int kc, int rowb, int groups, int Cin, i
         const long long rounds = (tiles + sms - 1) / sms;
         const double fill = (double)tiles / ((double)rounds * sms);
         const double edge = (double)H / ((double)((H + TR - 1) / TR) * TR);
-        const double halo = (double)TR / (TR + 2);
+        const double halo = (double)TR / rows_staged(MT);
         const double eff = fill * edge * halo;
         if (eff > best_eff + 1e-9) {
             best_eff = eff;
@@ -585,9 +698,10 @@ static bool tc_geometry(int Cg, int NB, int kc, int rowb, int groups, int Cin, i
         }
     }
     if (best_mt == 0) return false;
+    const size_t fixed = fixed_of(best_mt);
     g.MT = best_mt;
-    g.TR = 4 * g.MT;
-    g.THh = g.TR + 2;
+    g.TR = rows_out(g.MT);
+    g.THh = rows_staged(g.MT);
     g.tiles_x = tiles_x;
     g.tiles_y = (H + g.TR - 1) / g.TR;
     g.ntiles = g.tiles_x * g.tiles_y * Nimg;
@@ -619,23 +733,24 @@ static PFN_cuTensorMapEncodeTiled_v12000 tc_tensor_map_encoder()
 }
 
 // a.x and a.y point to fp32 or (for OP = OpBF16, YBF16) bf16 NHWC tensors.
-template <int CG, class OP, bool YBF16>
+template <int CG, class OP, bool YBF16, bool RSN = false>
 static cudaError_t launch_tc_cg(const ConvArgs &a, cudaStream_t st)
 {
-    constexpr int NB = (3 * CG + 15) / 16 * 16;
+    constexpr int NB = RSN ? (9 * CG + 15) / 16 * 16 : (3 * CG + 15) / 16 * 16;
     constexpr int OSZ = YBF16 ? 2 : 4;
     constexpr int OROWB = CG * OSZ;
+    if (RSN && (a.R != 3 || a.S != 3)) return cudaErrorNotSupported;
     tc::TcGeom g;
     const int groups = (a.Cout + CG - 1) / CG;
-    if (!tc_geometry(CG, NB, OP::KC, OP::ROWB * OP::SUB, groups, a.Cin, a.R * a.S, a.H, a.W, a.N, OP::X3, g))
+    if (!tc_geometry(CG, NB, OP::KC, OP::ROWB * OP::SUB, groups, a.Cin, a.R * a.S, a.H, a.W, a.N, OP::X3, RSN, g))
         return cudaErrorNotSupported;
     if ((long long)g.tiles_x * g.tiles_y * a.N > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     PFN_cuTensorMapEncodeTiled_v12000 encode = tc_tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
     // NHWC activations as a 4-D tensor (C, W, H, N); box = the channels of
     // one sub-buffer (32 fp32 or 16 bf16: one swizzled row per pixel;
-    // channels past Cin read as zero) x 32 padded columns x (TR + 2) rows of
-    // one image
+    // channels past Cin read as zero) x 32 padded columns x THh (= TR + 2)
+    // rows of one image
     CUtensorMap tm;
     const cuuint64_t dims[4] = {(cuuint64_t)a.Cin, (cuuint64_t)a.W, (cuuint64_t)a.H, (cuuint64_t)a.N};
     const cuuint64_t strides[3] = {(cuuint64_t)a.Cin * OP::ESZ, (cuuint64_t)a.W * a.Cin * OP::ESZ,
@@ -669,11 +784,11 @@ static cudaError_t launch_tc_cg(const ConvArgs &a, cudaStream_t st)
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     static KernelCache cache;
-    e = ensure_dynamic_smem(cache, dev, conv_tc_kernel<CG, OP, YBF16>, (int)g.smem_bytes);
+    e = ensure_dynamic_smem(cache, dev, conv_tc_kernel<CG, OP, YBF16, RSN>, (int)g.smem_bytes);
     if (e != cudaSuccess) return e;
     const int per_group = device_sm_count() / groups > 0 ? device_sm_count() / groups : 1;
     const int grid = g.ntiles < per_group ? g.ntiles : per_group;
-    conv_tc_kernel<CG, OP, YBF16><<<dim3(grid, groups), tc::NTHREADS, g.smem_bytes, st>>>(
+    conv_tc_kernel<CG, OP, YBF16, RSN><<<dim3(grid, groups), tc::NTHREADS, g.smem_bytes, st>>>(
         tm, tmo, a.w, a.b, a.y, a.H, a.W, a.Cin, a.Cout, a.R, a.S, a.act, g, device_status_ptr(), 1000000000ull);
     return cudaGetLastError();
 }
@@ -690,6 +805,8 @@ static cudaError_t launch_tc_groups(const ConvArgs &a, cudaStream_t st)
     if (a.Cout > 16) e = launch_tc_cg<32, OP, YBF16>(a, st);
     if (e == cudaErrorNotSupported && a.Cout > 8) e = launch_tc_cg<16, OP, YBF16>(a, st);
     if (e == cudaErrorNotSupported && a.Cout > 4) e = launch_tc_cg<8, OP, YBF16>(a, st);
+    // 4 or fewer channels with 3 x 3 filters: all nine taps in N
+    if (e == cudaErrorNotSupported && a.Cout <= 4) e = launch_tc_cg<4, OP, YBF16, true>(a, st);
     if (e == cudaErrorNotSupported) e = launch_tc_cg<4, OP, YBF16>(a, st);
     return e;
 }

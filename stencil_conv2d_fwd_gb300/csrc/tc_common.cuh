@@ -287,6 +287,7 @@ __device__ __forceinline__ void stage_filter_bank_taps_in_n(const float *raw, ui
                                                             int Cin, int nk, int lt, int LT)
 {
     constexpr int NB = (9 * CG + 15) / 16 * 16;
+    constexpr int RB = OP::X3 ? 2 * NB : NB;   // rows per (k, cb) block (X3: heads, then remainders)
     constexpr int CU = OP::KC / 2;
     const int units = CG * 2 * nk;
     for (int u = lt; u < units; u += LT) {
@@ -302,20 +303,27 @@ __device__ __forceinline__ void stage_filter_bank_taps_in_n(const float *raw, ui
 #pragma unroll
         for (int t = 0; t < 9; ++t) {
             uint4 o;
+            const int at = (k * 2 + cb) * RB + t * CG + co;
             if constexpr (CU == 4) {
                 o = make_uint4(__float_as_uint(f[t]), __float_as_uint(f[9 + t]), __float_as_uint(f[18 + t]),
                                __float_as_uint(f[27 + t]));
+                if constexpr (OP::X3) {
+                    bank[at + NB] = make_uint4(tf32_rest(o.x), tf32_rest(o.y), tf32_rest(o.z), tf32_rest(o.w));
+                    o = make_uint4(tf32_head(o.x), tf32_head(o.y), tf32_head(o.z), tf32_head(o.w));
+                }
             } else {
                 o = make_uint4(pack_bf16(f[t], f[9 + t]), pack_bf16(f[18 + t], f[27 + t]), pack_bf16(f[36 + t], f[45 + t]),
                                pack_bf16(f[54 + t], f[63 + t]));
             }
-            bank[(k * 2 + cb) * NB + t * CG + co] = o;
+            bank[at] = o;
         }
     }
     constexpr int PADN = NB - 9 * CG;
     if constexpr (PADN > 0) {
-        for (int e = lt; e < nk * 2 * PADN; e += LT)
-            bank[(e / PADN) * NB + 9 * CG + e % PADN] = make_uint4(0u, 0u, 0u, 0u);
+        for (int e = lt; e < nk * 2 * PADN; e += LT) {
+            bank[(e / PADN) * RB + 9 * CG + e % PADN] = make_uint4(0u, 0u, 0u, 0u);
+            if constexpr (OP::X3) bank[(e / PADN) * RB + NB + 9 * CG + e % PADN] = make_uint4(0u, 0u, 0u, 0u);
+        }
     }
 }
 

@@ -111,11 +111,14 @@ def test_x3_rejects_what_it_does_not_run(cuda_dev, sc):
     assert sc.conv2d_fwd_tc_x3(x, w, None, y, 1, 8, 8, 6, 4, 3, 3, 0) == sc.SC_ERR_UNSUPPORTED
     assert sc.conv2d_fwd_tc_x3(x, w, None, y, 1, 8, 8, 4, 4, 5, 5, 0) == sc.SC_ERR_UNSUPPORTED
     # heads and remainders of the filters do not fit in shared memory (plain
-    # TF32 still runs this shape)
+    # TF32 still runs this shape; with 4 output channels the nine-taps-in-N
+    # layout's smaller stages leave room, so 8 are used here)
     xb = torch.zeros(8 * 8 * 320, device=cuda_dev)
-    wb = torch.zeros(4 * 320 * 9, device=cuda_dev)
-    assert sc.conv2d_fwd_tc_x3(xb, wb, None, y, 1, 8, 8, 320, 4, 3, 3, 0) == sc.SC_ERR_UNSUPPORTED
-    assert sc.conv2d_fwd_tc(xb, wb, None, y, 1, 8, 8, 320, 4, 3, 3, 0) == sc.SC_OK
+    wb = torch.zeros(8 * 320 * 9, device=cuda_dev)
+    y8 = torch.zeros(8 * 8 * 8, device=cuda_dev)
+    assert sc.conv2d_fwd_tc_x3(xb, wb, None, y8, 1, 8, 8, 320, 8, 3, 3, 0) == sc.SC_ERR_UNSUPPORTED
+    assert sc.conv2d_fwd_tc(xb, wb, None, y8, 1, 8, 8, 320, 8, 3, 3, 0) == sc.SC_OK
+    assert sc.conv2d_fwd_tc_x3(xb, wb, None, y8, 1, 8, 8, 320, 4, 3, 3, 0) == sc.SC_OK
     wu = torch.zeros(4 * 4 * 9 + 1, device=cuda_dev)[1:]
     assert sc.conv2d_fwd_tc_x3(x, wu, None, y, 1, 8, 8, 4, 4, 3, 3, 0) == sc.SC_ERR_ALIGN
     torch.cuda.synchronize()
