@@ -110,10 +110,12 @@ int conv2d_fwd_tc(const float *x, const float *w, const float *b, float *y,
  * in a separate accumulator added once at the end (split or "3xTF32"
  * arithmetic: Ootomo and Yokota, "Recovering single precision accuracy from
  * Tensor Cores while surpassing the FP32 theoretical peak performance",
- * 2022).  The dropped lo(x) lo(w) and the remainders' own TF32 rounding keep
- * every product within about 3 * 2^-20 of exact, so the result meets
- * conv2d_fwd's bound |y - y_ref| <= 1e-5 * (sum|x * w| + |b|).  Three MMAs
- * per product: a separate variant, not conv2d_fwd's FP32 FMA path.
+ * 2022).  The dropped lo(x) lo(w) and the remainders' own TF32 truncation
+ * keep every product within about 3 * 2^-20 of exact, so the result meets
+ * conv2d_fwd's bound |y - y_ref| <= 1e-5 * (sum|x * w| + |b|).  Three TF32
+ * products per product (issued as two MMAs, the filters' heads and
+ * remainders side by side in N): a separate variant, not conv2d_fwd's FP32
+ * FMA path.
  * Arguments, layouts and errors as for conv2d_fwd_tc.  Both the filters'
  * heads and remainders stay resident in shared memory, so the supported
  * Cin is about half of conv2d_fwd_tc's (about 250).

@@ -1,4 +1,4 @@
-"""conv2d_fwd_tc_x3 (tcgen05, split-TF32 operands: three MMAs per product,
+"""conv2d_fwd_tc_x3 (tcgen05, split-TF32 operands: three TF32 products per product,
 head and correction accumulators) vs the fp64 oracle, at conv2d_fwd's own
 fp32 bound |y - y_ref| <= 1e-5 * (sum |x * w| + |b|) per element.  One test
 also runs plain TF32 (conv2d_fwd_tc) on the same data to show that bound is
