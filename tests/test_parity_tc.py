@@ -40,6 +40,12 @@ SHAPES = [
     (1, 16, 48, 11, 257, 3, 3),
     (1, 8, 16, 12, 17, 1, 1),
     (1, 8, 12, 12, 17, 3, 1),
+    # 4 output channels, 3 x 3: all nine taps in N (an image shorter than a
+    # tile, Cin not a multiple of 8, two 32-channel stages, N > 1)
+    (2, 8, 4, 7, 29, 3, 3),
+    (1, 12, 4, 5, 200, 3, 3),
+    (1, 64, 4, 37, 95, 3, 3),
+    (3, 16, 4, 50, 31, 3, 3),
     # filters too large for 32-channel groups: 16- and 8-channel groups
     (1, 128, 32, 9, 40, 3, 3),
     (1, 256, 12, 6, 33, 3, 3),

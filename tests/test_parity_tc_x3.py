@@ -43,6 +43,11 @@ SHAPES = [
     (1, 8, 16, 12, 17, 1, 1),
     (1, 8, 12, 12, 17, 3, 1),
     (1, 40, 8, 7, 61, 1, 3),
+    # 4 output channels, 3 x 3: all nine taps in N
+    (2, 8, 4, 7, 29, 3, 3),
+    (1, 12, 4, 5, 200, 3, 3),
+    (1, 64, 4, 37, 95, 3, 3),
+    (3, 16, 4, 50, 31, 3, 3),
     # filters too large for 32-channel groups: 16-, 8- and 4-channel groups
     (1, 64, 64, 9, 40, 3, 3),
     (1, 128, 32, 9, 40, 3, 3),
