@@ -43,7 +43,7 @@
 // mbarriers:
 //  * all warps first stage the group's filters (bulk copy of the OIHW rows,
 //    then a transpose in shared memory into the B layout).
-//  * producer (warp 4, one lane): per stage one TMA box of (32 channels, 32 pixels, TR + 2 rows) of the
+//  * producer (warp 4, one lane): per stage one TMA box of (32 channels, 32 pixels, THh rows) of the
 //    tile's padded activations; the TMA zero fill outside the image (and
 //    past Cin) is the convolution's zero padding.  A stage buffer is
 //    refilled once the MMAs that read it have completed (`empty`).
@@ -52,13 +52,22 @@
 //    and after a tile's last stage commits to the tile's accumulator
 //    barrier.  Each barrier wait leaves the tensor core idle for ~100-200
 //    clocks, so stages are large (32 channels).
-//  * epilogue (warps 0-3, one TMEM lane quadrant each): waits for a tile's
-//    accumulators, reads the three s-blocks with tcgen05.ld, sums them with
-//    lane shifts, transposes through a swizzled per-warp shared-memory
-//    buffer so that each store instruction writes whole pixel records, adds
-//    bias, applies ReLU, writes NHWC, and frees the accumulator buffer.
-//    Accumulators are double-buffered in tensor memory, so a tile's epilogue
-//    overlaps the next tile's MMAs.
+//  * epilogue (warps 0-3 and 6-9, one TMEM lane quadrant each, the two sets
+//    on alternate M-tiles): waits for a tile's accumulators, reads the
+//    three s-blocks with tcgen05.ld, sums them with lane shifts, transposes
+//    through a swizzled per-warp shared-memory buffer so that each store
+//    instruction writes whole pixel records, adds bias, applies ReLU,
+//    writes NHWC, and frees the accumulator buffer.  Accumulators are
+//    double-buffered in tensor memory, so a tile's epilogue overlaps the
+//    next tile's MMAs.
+// Two modes change this (template parameters of the kernel):
+//  * split TF32 (OpTF32x3): warps 6-9 write each stage's TF32 remainders
+//    instead (the MMA reads the copied values as their TF32 heads); every
+//    (K step, tap) issues x_hi [w_hi | w_lo] and x_lo w_hi into a head and
+//    a correction accumulator, which the epilogue adds (warps 0-3 alone).
+//  * nine taps in N (RSN, 4-channel groups, 3 x 3): one MMA per K step and
+//    M-tile over the tile's staged rows; the epilogue sums the horizontal
+//    taps by lane shifts and the vertical ones through shared memory.
 // Every wait is bounded in time; on expiry the CTA records
 // SC_ERR_DEVICE_TIMEOUT, lets its own copies and MMAs land, frees tensor
 // memory and returns.
