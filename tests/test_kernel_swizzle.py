@@ -238,3 +238,35 @@ def test_tma_even_pixel_run_would_conflict(swz):
     which the swizzle cannot separate: the kernel uses odd runs."""
     chunks = [((lane * 4) * 32 + 16 * (0 ^ swz.h_tma_key(lane * 4, 8))) // 16 for lane in range(32)]
     assert not phases_conflict_free(chunks)
+
+
+def _c1_tile_store_chunks(j, g, staggered):
+    """16-byte chunk (of the warp's 8 KB output buffer) that each lane of the
+    tiled single-channel kernel writes at step (g, j): lane = 4 pl + cl, pixel
+    p = 8 pl + jj (jj = j, or j ^ 4 for odd pixel lanes when staggered),
+    chunk q = 4 g + cl of its 128-byte row, swizzled 128-byte style
+    (q ^ (p mod 8))."""
+    out = []
+    for lane in range(32):
+        cl, pl = lane & 3, lane >> 2
+        jj = (j ^ 4) if (staggered and pl & 1) else j
+        p = 8 * pl + jj
+        q = 4 * g + cl
+        out.append(p * 8 + (q ^ (p & 7)))
+    return out
+
+
+def test_c1_tile_output_writes_conflict_free_and_one_to_one():
+    seen = []
+    for g in range(2):
+        for j in range(8):
+            ch = _c1_tile_store_chunks(j, g, staggered=True)
+            assert phases_conflict_free(ch), (g, j)
+            seen += ch
+    # every (pixel, chunk) slot of the 64 x 128-byte row is written exactly once
+    assert sorted(seen) == list(range(64 * 8))
+
+
+def test_c1_tile_unstaggered_writes_would_conflict():
+    # pixels j and 8 + j of the two pixel lanes in a phase share a swizzle row
+    assert not phases_conflict_free(_c1_tile_store_chunks(0, 0, staggered=False))
