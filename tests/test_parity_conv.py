@@ -159,7 +159,7 @@ def test_single_input_channel_shapes(oracle_mod, cuda_dev, sc, shape):
 
 
 @pytest.mark.parametrize("shape", [(2, 8, 12, 9, 20, 3, 3), (1, 1, 16, 13, 37, 5, 5), (1, 16, 4, 17, 9, 3, 3),
-                                   (1, 1, 1, 10, 11, 3, 3)])
+                                   (1, 1, 1, 10, 11, 3, 3), (2, 1, 32, 9, 68, 5, 5)])
 def test_nchw_layout(oracle_mod, cuda_dev, sc, shape):
     N, Cin, Cout, H, W, R, S_ = shape
     c = S.conv_case(300 + Cin + Cout, N, Cin, Cout, H, W, R, S_, act=1)
