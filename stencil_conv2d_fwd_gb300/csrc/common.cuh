@@ -44,6 +44,17 @@ SC_HD int swz_col(int row, int c, int log2_chunks_per_row)
 // stored at chunk q ^ tma_swz_key(p, c_sh) of that pixel.
 SC_HD int tma_swz_key(int p, int c_sh) { return (p * c_sh / 32) & (c_sh / 4 - 1); }
 
+// Physical 16-byte chunk of logical chunk L of a staged input row of the
+// tiled single-channel kernel (conv_c1.cu).  A thread's window starts 2
+// chunks after its left neighbour's, so without a swizzle pixel lanes pl and
+// pl + 4 of a quarter-warp read the same bank group.  Swapping the two
+// chunks of each pair in every odd group of 8 ("CUDA共有メモリのスウィズリング":
+// chunk x of row y at x XOR y, with y = bit 3 of L and x's lowest bit) puts
+// the 8 pixel lanes' chunks in 8 distinct bank groups for every chunk of the
+// window.  It only swaps chunks 2k and 2k + 1, so it is one-to-one on a row
+// of an even number of chunks.
+SC_HD int c1_band_chunk(int L) { return L ^ ((L >> 3) & 1); }
+
 #if defined(__CUDACC__)
 
 // ---------------------------------------------------------------------------
@@ -208,6 +219,15 @@ __device__ __forceinline__ void tma_store_4d(const void *tmap, uint32_t src, int
     asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];\n" ::"l"(
                      reinterpret_cast<unsigned long long>(tmap)),
                  "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(src)
+                 : "memory");
+}
+
+// 5-D tiled TMA store, as tma_store_4d.
+__device__ __forceinline__ void tma_store_5d(const void *tmap, uint32_t src, int c0, int c1, int c2, int c3, int c4)
+{
+    asm volatile("cp.async.bulk.tensor.5d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4, %5}], [%6];\n" ::"l"(
+                     reinterpret_cast<unsigned long long>(tmap)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(src)
                  : "memory");
 }
 

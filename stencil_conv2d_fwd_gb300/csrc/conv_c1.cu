@@ -500,7 +500,11 @@ __global__ void __launch_bounds__(32 * kC1TileWarps, kC1TileCtas)
     __shared__ __align__(16) float ws[K * K * CO];
     __shared__ __align__(16) float bs[CO];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int cl = lane & 3, pl = lane >> 2;   // 4 channel lanes x 8 pixel lanes
+    // 4 channel lanes x 8 pixel lanes; the 8 lanes of a quarter-warp share
+    // a channel lane, so a filter load asks for one 16-byte chunk per
+    // quarter-warp (2 shared-memory wavefronts where one chunk per lane of
+    // a quarter takes 4)
+    const int cl = lane >> 3, pl = lane & 7;
     const int co0 = blockIdx.y * CO;
     const int n = blockIdx.z;
     const int ct = blockIdx.x % col_tiles, rt = blockIdx.x / col_tiles;
@@ -533,7 +537,8 @@ __global__ void __launch_bounds__(32 * kC1TileWarps, kC1TileCtas)
             const int r = e / CPR, q = e % CPR;
             const int iy = y0 - HALO + r, ix = tx0 - 4 + 4 * q;
             const bool ok = iy >= 0 && iy < H && ix >= 0 && ix + 3 < W;
-            cp_async16(smem_u32(tile + r * kC1TilePitch + 4 * q), ok ? xn + (long long)iy * W + ix : x, ok ? 16 : 0);
+            cp_async16(smem_u32(tile + r * kC1TilePitch + 4 * c1_band_chunk(q)), ok ? xn + (long long)iy * W + ix : x,
+                       ok ? 16 : 0);
         }
         cp_async_commit();
     };
@@ -543,7 +548,11 @@ __global__ void __launch_bounds__(32 * kC1TileWarps, kC1TileCtas)
     __syncthreads();
 
     const int xw = tx0 + warp * 64;             // the warp's first column
-    const int cb = warp * 64 + pl * PX;         // staged column of this thread's pixel x - 4
+    // staged 16-byte chunks of this thread's window (image columns x - 4 ..
+    // x + 11): logical chunks 16 * warp + 2 * pl + q, q = 0..3
+    int woff[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) woff[q] = 4 * c1_band_chunk(16 * warp + 2 * pl + q);
     const uint32_t buf = obase + (uint32_t)(warp * kC1TileOutBuf);
     for (int i = 0; i < nrows; ++i) {
         const int oy = y0 + i;
@@ -566,11 +575,11 @@ __global__ void __launch_bounds__(32 * kC1TileWarps, kC1TileCtas)
 #pragma unroll
         for (int ky = 0; ky < K; ++ky) {
             // image columns x - 4 .. x + 11 of input row oy - HALO + ky
-            const float *trow = tile + (i + ky) * kC1TilePitch + cb;
+            const float *trow = tile + (i + ky) * kC1TilePitch;
             float win[16];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const float4 t = *reinterpret_cast<const float4 *>(trow + 4 * q);
+                const float4 t = *reinterpret_cast<const float4 *>(trow + woff[q]);
                 win[4 * q] = t.x;
                 win[4 * q + 1] = t.y;
                 win[4 * q + 2] = t.z;
@@ -605,21 +614,21 @@ __global__ void __launch_bounds__(32 * kC1TileWarps, kC1TileCtas)
         if (lane == 0) bulk_wait_read<0>();   // the store that last read this buffer is done
         __syncwarp();
         if (xw < W) {
-            // lanes of odd pixel lanes write pixel j ^ 4 when the others
-            // write pixel j: the two pixel lanes of an 8-lane phase then
-            // land in different swizzle rows (no bank conflict)
-            const bool odd = pl & 1;
+            // the buffer holds the warp's 64 pixels in the order the output
+            // copy's box walks them: pixel 8 * pl + j in 128-byte row
+            // 8 * j + pl, 16-byte chunk q at q ^ pl (the 128-byte TMA
+            // swizzle of that row), so the 8 pixel lanes of a quarter-warp
+            // write 8 distinct bank groups
 #pragma unroll
             for (int g = 0; g < 2; ++g)
 #pragma unroll
                 for (int j = 0; j < PX; ++j) {
-                    const int jj = odd ? (j ^ 4) : j;
-                    const int p = pl * PX + jj;   // pixel of the warp's row
-                    const int q = g * 4 + cl;     // 16-byte chunk: channels 4q .. 4q + 3
+                    const int q = g * 4 + cl;   // 16-byte chunk: channels 4q .. 4q + 3
                     float o[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) o[e] = relu_if(odd ? acc[4 * g + e][j ^ 4] : acc[4 * g + e][j], act);
-                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(buf + p * 128 + ((q ^ (p & 7)) << 4)),
+                    for (int e = 0; e < 4; ++e) o[e] = relu_if(acc[4 * g + e][j], act);
+                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(buf + (8 * j + pl) * 128 +
+                                                                                     ((q ^ pl) << 4)),
                                  "f"(o[0]), "f"(o[1]), "f"(o[2]), "f"(o[3])
                                  : "memory");
                 }
@@ -627,7 +636,7 @@ __global__ void __launch_bounds__(32 * kC1TileWarps, kC1TileCtas)
         fence_proxy_async_smem();   // these writes -> visible to the copy
         __syncwarp();
         if (lane == 0 && xw < W) {
-            tma_store_4d(&tmy, buf, co0, xw, oy, n);
+            tma_store_5d(&tmy, buf, co0, xw / 8, 0, oy, n);
             bulk_commit();
         }
     }
@@ -649,13 +658,18 @@ static cudaError_t launch_c1_tile(const ConvArgs &a, cudaStream_t st)
     if (rows_per_cta > 48) rows_per_cta = 48;   // bounds the staged tile
     const long long nb = (long long)col_tiles * ((a.H + rows_per_cta - 1) / rows_per_cta);
     if (nb > 0x7fffffffLL || groups > 65535 || a.N > 65535) return cudaErrorInvalidConfiguration;
+    // The output as a 5-D tensor (channel, pixel group of 8, pixel in the
+    // group, row, image): the box (32 channels, 8 groups, 8 pixels) of a
+    // warp's row lands in shared memory with group fastest, i.e. pixel
+    // 8 * g + j in 128-byte row 8 * j + g.  Needs W % 8 == 0.
+    if (a.W % 8) return cudaErrorNotSupported;
     CUtensorMap tm;
-    const cuuint64_t dims[4] = {(cuuint64_t)a.Cout, (cuuint64_t)a.W, (cuuint64_t)a.H, (cuuint64_t)a.N};
-    const cuuint64_t strides[3] = {(cuuint64_t)a.Cout * 4, (cuuint64_t)a.W * a.Cout * 4,
+    const cuuint64_t dims[5] = {(cuuint64_t)a.Cout, (cuuint64_t)(a.W / 8), 8, (cuuint64_t)a.H, (cuuint64_t)a.N};
+    const cuuint64_t strides[4] = {(cuuint64_t)a.Cout * 32, (cuuint64_t)a.Cout * 4, (cuuint64_t)a.W * a.Cout * 4,
                                    (cuuint64_t)a.H * a.W * a.Cout * 4};
-    const cuuint32_t box[4] = {32, 64, 1, 1};
-    const cuuint32_t estr[4] = {1, 1, 1, 1};
-    if (encode(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.y, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    const cuuint32_t box[5] = {32, 8, 8, 1, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    if (encode(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, a.y, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorNotSupported;

@@ -25,25 +25,48 @@ def swz(tmp_path_factory):
     src.write_text(f'#include "{HDR}"\n'
                    'extern "C" int h_swz16(int i, int L) { return sc::swz16(i, L); }\n'
                    'extern "C" int h_swz_col(int r, int c, int L) { return sc::swz_col(r, c, L); }\n'
-                   'extern "C" int h_tma_key(int p, int c) { return sc::tma_swz_key(p, c); }\n')
+                   'extern "C" int h_tma_key(int p, int c) { return sc::tma_swz_key(p, c); }\n'
+                   'extern "C" int h_c1_band_chunk(int L) { return sc::c1_band_chunk(L); }\n')
     so = d / "libswz.so"
     subprocess.run(["g++", "-std=c++17", "-O1", "-fPIC", "-shared", str(src), "-o", str(so)], check=True)
     lib = ctypes.CDLL(str(so))
     lib.h_swz16.argtypes = [ctypes.c_int, ctypes.c_int]
     lib.h_swz_col.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
     lib.h_tma_key.argtypes = [ctypes.c_int, ctypes.c_int]
+    lib.h_c1_band_chunk.argtypes = [ctypes.c_int]
     return lib
 
 
-def wavefronts_128bit(chunks):
-    """Shared-memory wavefronts for one warp-wide 16-byte access: distinct
-    16-byte chunks are served 8 per wavefront, at most one per 128-byte bank
-    window position (chunk mod 8)."""
-    uniq = set(chunks)
+def phase_wavefronts(chunks):
+    """Wavefronts for one group of lanes served together: its distinct 16-byte
+    chunks take one wavefront per chunk that shares a bank group (chunk mod
+    8) with another."""
     per_pos = {}
-    for c in uniq:
+    for c in set(chunks):
         per_pos[c % 8] = per_pos.get(c % 8, 0) + 1
     return max(per_pos.values())
+
+
+def wavefronts_128bit(chunks_by_lane, ideal=False):
+    """Shared-memory wavefronts of one warp-wide 16-byte load on GB300, as
+    measured with ncu (l1tex__data_pipe_lsu_wavefronts_mem_shared_op_ld) on
+    probe kernels of fixed lane -> chunk patterns: when no quarter-warp (8
+    consecutive lanes) asks for more than 2 distinct chunks, each half-warp
+    is served in one wavefront (2 in all, also for a pure broadcast);
+    otherwise each quarter-warp takes its own (4 in all).  A bank-group
+    clash inside the group served together adds wavefronts (ideal=True
+    leaves them out)."""
+    assert len(chunks_by_lane) == 32
+    quarters = [chunks_by_lane[q:q + 8] for q in range(0, 32, 8)]
+    if all(len(set(q)) <= 2 for q in quarters):
+        groups = [chunks_by_lane[:16], chunks_by_lane[16:]]
+    else:
+        groups = quarters
+    return sum(1 if ideal else phase_wavefronts(g) for g in groups)
+
+
+def conflict_free_128bit(chunks_by_lane):
+    return wavefronts_128bit(chunks_by_lane) == wavefronts_128bit(chunks_by_lane, ideal=True)
 
 
 def min_wavefronts_128bit(chunks):
@@ -54,10 +77,29 @@ def phases_conflict_free(chunks_by_lane):
     """A 16-byte shared access is served 8 lanes at a time: in each group of 8
     consecutive lanes, distinct chunks must sit in distinct bank groups."""
     for q in range(0, len(chunks_by_lane), 8):
-        ph = set(chunks_by_lane[q:q + 8])
-        if len({c % 8 for c in ph}) != len(ph):
+        if phase_wavefronts(chunks_by_lane[q:q + 8]) != 1:
             return False
     return True
+
+
+@pytest.mark.parametrize("pattern,want", [
+    (lambda l: l, 4),                      # 32 distinct contiguous chunks
+    (lambda l: 0, 2),                      # one chunk for the whole warp
+    (lambda l: l & 3, 4),                  # 4 chunks, lanes interleaved
+    (lambda l: l >> 3, 2),                 # one chunk per quarter-warp
+    (lambda l: 2 * (l >> 2), 2),           # 8 chunks 2 apart, 4 lanes each
+    (lambda l: l >> 2, 2),                 # 8 contiguous chunks, 4 lanes each
+    (lambda l: l & 7, 4),                  # 8 contiguous chunks, interleaved
+    (lambda l: (l & 3) + 4 * (l >> 4), 4),
+    (lambda l: 4 * (l & 1), 2),
+    (lambda l: l >> 4, 2),
+])
+def test_wavefront_model_reproduces_the_measured_probe_counts(pattern, want):
+    """The probe kernels' measured wavefronts per load (no bank conflicts in
+    any of them)."""
+    chunks = [pattern(l) for l in range(32)]
+    assert wavefronts_128bit(chunks) == want
+    assert conflict_free_128bit(chunks)
 
 
 @pytest.mark.parametrize("L", [1, 2, 3, 4, 5])
@@ -118,8 +160,7 @@ def test_general_conv_pixel_reads_conflict_free(swz, K, F_TB, W_T, TH, TW, C_SH)
                         pl = lane // c["T_X"]
                         cx0 = (warp % c["WPR"]) * c["WARP_COLS"] + pl * W_T
                         chunks.append(cb * c["PLANE"] + (ry + r) * c["TWP"] + col_map(swz, W_T, cx0 + j))
-                    assert wavefronts_128bit(chunks) == min_wavefronts_128bit(chunks), \
-                        (warp, cb, r, j)
+                    assert conflict_free_128bit(chunks), (warp, cb, r, j)
                     assert phases_conflict_free(chunks), (warp, cb, r, j)
 
 
@@ -139,10 +180,11 @@ def test_general_conv_tile_writes_stay_in_tile_and_are_one_to_one(swz, K, F_TB, 
             # one warp instruction: conflict-free when all 32 lanes copy, and in
             # every 8-lane phase; the partial last instruction of a row may take
             # one extra wavefront
-            slack = 0 if len(chunks) == 32 else 1
-            assert wavefronts_128bit(chunks) <= min_wavefronts_128bit(chunks) + slack
             if len(chunks) == 32:
+                assert conflict_free_128bit(chunks)
                 assert phases_conflict_free(chunks)
+            else:
+                assert phase_wavefronts(chunks) <= min_wavefronts_128bit(chunks) + 1
             phys += chunks
     assert len(set(phys)) == len(phys) == c["CB"] * c["THh"] * c["TWU"]   # one-to-one
     assert max(phys) < (c["CB"] * c["PLANE"] + 7) // 8 * 8                 # inside the stage's tile
@@ -151,8 +193,8 @@ def test_general_conv_tile_writes_stay_in_tile_and_are_one_to_one(swz, K, F_TB, 
 def test_odd_stride_needs_no_swizzle_and_xor_would_hurt(swz):
     """W_T = 7: plain columns 7k are in 8 different bank groups; XORed ones are not."""
     plain = [7 * k for k in range(8)]
-    assert wavefronts_128bit(plain) == 1
-    assert wavefronts_128bit([swz.h_swz16(cc, 3) for cc in plain]) > 1
+    assert phase_wavefronts(plain) == 1
+    assert phase_wavefronts([swz.h_swz16(cc, 3) for cc in plain]) > 1
 
 
 def test_general_conv_unswizzled_pixel_reads_would_conflict():
@@ -160,7 +202,7 @@ def test_general_conv_unswizzled_pixel_reads_would_conflict():
     so (for W_T = 8) every lane lands on the same bank window position."""
     W_T, PXL = 8, 4
     chunks = [pl * W_T for pl in range(PXL) for _ in range(8)]
-    assert wavefronts_128bit(chunks) == PXL > min_wavefronts_128bit(chunks)
+    assert phase_wavefronts(chunks) == PXL > min_wavefronts_128bit(chunks)
 
 
 def bank_ways_32bit(word_addrs):
@@ -240,33 +282,74 @@ def test_tma_even_pixel_run_would_conflict(swz):
     assert not phases_conflict_free(chunks)
 
 
-def _c1_tile_store_chunks(j, g, staggered):
-    """16-byte chunk (of the warp's 8 KB output buffer) that each lane of the
-    tiled single-channel kernel writes at step (g, j): lane = 4 pl + cl, pixel
-    p = 8 pl + jj (jj = j, or j ^ 4 for odd pixel lanes when staggered),
-    chunk q = 4 g + cl of its 128-byte row, swizzled 128-byte style
-    (q ^ (p mod 8))."""
-    out = []
-    for lane in range(32):
-        cl, pl = lane & 3, lane >> 2
-        jj = (j ^ 4) if (staggered and pl & 1) else j
-        p = 8 * pl + jj
-        q = 4 * g + cl
-        out.append(p * 8 + (q ^ (p & 7)))
-    return out
+# ---------------------------------------------------------------------------
+# conv_c1.cu, conv_c1_tile_kernel: lane = 8 * cl + pl (4 channel lanes, one
+# per quarter-warp; 8 pixel lanes), 8 pixels 8 * pl + j and 8 output channels
+# per thread, staged input rows of 66 16-byte chunks, one 8 KB output buffer
+# per warp.
+
+def _c1_lane(lane):
+    return lane >> 3, lane & 7          # (cl, pl)
+
+
+@pytest.mark.parametrize("warp", range(4))
+@pytest.mark.parametrize("row", range(3))
+def test_c1_tile_band_reads_conflict_free(swz, warp, row):
+    """Window chunk q (0..3) of row `row`: logical chunk 16 warp + 2 pl + q,
+    stored at c1_band_chunk of it; each quarter-warp asks for its 8 pixel
+    lanes' chunks in 8 distinct bank groups."""
+    for q in range(4):
+        chunks = []
+        for lane in range(32):
+            cl, pl = _c1_lane(lane)
+            chunks.append(66 * row + swz.h_c1_band_chunk(16 * warp + 2 * pl + q))
+        assert conflict_free_128bit(chunks), q
+        assert wavefronts_128bit(chunks) == 4
+
+
+def test_c1_tile_band_unswizzled_reads_would_conflict():
+    chunks = [2 * _c1_lane(l)[1] for l in range(32)]
+    assert not conflict_free_128bit(chunks)
+
+
+def test_c1_band_chunk_is_one_to_one_on_a_row(swz):
+    assert sorted(swz.h_c1_band_chunk(L) for L in range(66)) == list(range(66))
+
+
+def test_c1_tile_filter_reads_take_two_wavefronts():
+    """Filter unit 4 g + cl of a tap: one chunk per quarter-warp.  With the
+    channel lane in the low lane bits (cl = lane & 3) every quarter-warp
+    would ask for 4 chunks: 4 wavefronts instead of 2."""
+    for g in range(2):
+        assert wavefronts_128bit([4 * g + _c1_lane(l)[0] for l in range(32)]) == 2
+        assert wavefronts_128bit([4 * g + (l & 3) for l in range(32)]) == 4
+
+
+def _c1_tile_store_chunks(j, g):
+    """16-byte chunk of the warp's output buffer that each lane writes at
+    step (g, j): pixel 8 pl + j sits in 128-byte row 8 j + pl, its chunk
+    q = 4 g + cl at q ^ pl."""
+    return [(8 * j + pl) * 8 + ((4 * g + cl) ^ pl) for cl, pl in map(_c1_lane, range(32))]
 
 
 def test_c1_tile_output_writes_conflict_free_and_one_to_one():
     seen = []
     for g in range(2):
         for j in range(8):
-            ch = _c1_tile_store_chunks(j, g, staggered=True)
+            ch = _c1_tile_store_chunks(j, g)
             assert phases_conflict_free(ch), (g, j)
             seen += ch
-    # every (pixel, chunk) slot of the 64 x 128-byte row is written exactly once
     assert sorted(seen) == list(range(64 * 8))
 
 
-def test_c1_tile_unstaggered_writes_would_conflict():
-    # pixels j and 8 + j of the two pixel lanes in a phase share a swizzle row
-    assert not phases_conflict_free(_c1_tile_store_chunks(0, 0, staggered=False))
+def test_c1_tile_output_buffer_is_the_store_copy_box():
+    """The output copy's box is (32 channels, 8 pixel groups, 8 pixels of a
+    group), walked channel fastest, then group, then pixel: pixel 8 g + j is
+    128-byte row g + 8 j, and the 128-byte TMA swizzle moves its chunk q to
+    q ^ (row mod 8) = q ^ g, where the lanes wrote it (g = pl)."""
+    for g in range(8):
+        for j in range(8):
+            row = g + 8 * j
+            for q in range(8):
+                want = tma_swizzled_byte(row * 128 + 16 * q, 128)
+                assert want == row * 128 + 16 * (q ^ g)
