@@ -302,6 +302,14 @@ int sc_test_conv_wait_expiry(const float *x, const float *w, const float *b, flo
 int sc_test_stencil_wait_expiry(const float *in, float *out, int H, int W, int drop_copy,
                                 int timeout_us, sc_stream_t stream);
 
+/*
+ * sc_test_workspace_allocs: test hook, not part of the operation.  The
+ * number of temporary device buffers the library has taken from its memory
+ * pool since it was loaded (conv2d_fwd with SC_NCHW takes one per call);
+ * lets a test check that an entry point allocates nothing.
+ */
+long long sc_test_workspace_allocs(void);
+
 /* Floats of device scratch behind conv2d_fwd_nchw_noalloc (32 MiB). */
 #define SC_NOALLOC_SCRATCH_FLOATS (8u * 1024u * 1024u)
 
@@ -331,9 +339,12 @@ int sc_test_stencil_wait_expiry(const float *in, float *out, int H, int W, int d
  * has written first), so calls whose GPU work overlaps in time (different
  * streams, or different host threads on one device) race on it and must be
  * ordered by the caller.
+ * The device address is cached per device for the life of the process, so
+ * a cudaDeviceReset (which unloads the library's device memory) while the
+ * library is loaded is not supported.
  * Arguments, layout (x and y NCHW), supported shapes and status codes are
- * those of conv2d_fwd (a failed CUDA call returns SC_ERR_CUDA; its error
- * code is not recorded for sc_last_cuda_error).
+ * those of conv2d_fwd, checked by the same code; a failed CUDA call returns
+ * SC_ERR_CUDA and records its error code for sc_last_cuda_error.
  */
 int conv2d_fwd_nchw_noalloc(const float *x, const float *w, const float *b, float *y,
                             int N, int H, int W, int Cin, int Cout, int R, int S,

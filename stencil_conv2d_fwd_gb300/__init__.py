@@ -58,6 +58,7 @@ SIGNATURES = {
     "conv2d_fwd_nchw_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "sc_test_stencil_wait_expiry": (_I, [_P, _P, _I, _I, _I, _I, _P]),
     "sc_test_conv_wait_expiry": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
+    "sc_test_workspace_allocs": (ctypes.c_longlong, []),
 }
 SC_NOALLOC_SCRATCH_FLOATS = 8 * 1024 * 1024
 
@@ -208,6 +209,11 @@ def conv2d_fwd_nchw_noalloc(x, w, b, y, N, H, W, Cin, Cout, R, S, act=SC_ACT_NON
     """NCHW conv2d_fwd that allocates no device memory (see the header)."""
     return load().conv2d_fwd_nchw_noalloc(_ptr(x), _ptr(w), _ptr(b), _ptr(y), N, H, W, Cin, Cout, R, S,
                                           act, _stream(stream))
+
+
+def sc_test_workspace_allocs() -> int:
+    """Temporary device buffers taken by the library so far (test hook; see the header)."""
+    return load().sc_test_workspace_allocs()
 
 
 def sc_test_conv_wait_expiry(x, w, b, y, N, H, W, Cin, Cout, drop_copy, timeout_us, stream=None) -> int:

@@ -1,6 +1,7 @@
 // C-ABI of libstencilconv.so: argument validation, dispatch to the kernels,
 // the NCHW path through a stream-ordered temporary buffer, and the device
 // status word.  Declarations and contracts: include/stencilconv.h.
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <initializer_list>
@@ -19,11 +20,10 @@ thread_local int g_last_cuda_error = 0;
 // hanging; sc_last_device_status reads and clears it.
 __device__ int g_device_status;
 
-int cuda_fail(cudaError_t e)
-{
-    g_last_cuda_error = (int)e;
-    return SC_ERR_CUDA;
-}
+int cuda_fail(cudaError_t e) { return sc::record_cuda_error(e); }
+
+// Device allocations made by workspace_alloc (sc_test_workspace_allocs).
+std::atomic<long long> g_workspace_allocs{0};
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -56,6 +56,39 @@ int conv_nhwc_status(const sc::ConvArgs &a, cudaStream_t st)
 }  // namespace
 
 namespace sc {
+
+int record_cuda_error(cudaError_t e)
+{
+    g_last_cuda_error = (int)e;
+    return SC_ERR_CUDA;
+}
+
+int check_conv_args(const float *x, const float *w, const float *b, const float *y, int N, int H, int W, int Cin,
+                    int Cout, int R, int S, int layout, int act)
+{
+    if (!x || !w || !y) return SC_ERR_NULL;
+    const long long nx = checked_count({N, H, W, Cin});
+    const long long ny = checked_count({N, H, W, Cout});
+    const long long nw = checked_count({Cout, Cin, R, S});
+    if (nx < 0 || ny < 0 || nw < 0) return SC_ERR_SHAPE;
+    if (H > (1 << 30) || W > (1 << 30)) return SC_ERR_SHAPE;
+    if ((R & 1) == 0 || (S & 1) == 0 || R > 7 || S > 7) return SC_ERR_UNSUPPORTED;
+    if (layout != SC_NCHW && layout != SC_NHWC) return SC_ERR_UNSUPPORTED;
+    if (act != SC_ACT_NONE && act != SC_ACT_RELU) return SC_ERR_UNSUPPORTED;
+    if (Cin == 1) {
+        if (Cout != 1 && (Cout % 4) != 0) return SC_ERR_UNSUPPORTED;
+    } else {
+        if ((Cin % 4) != 0 || (Cout % 4) != 0) return SC_ERR_UNSUPPORTED;
+    }
+    if (Cin > 1 && !aligned16(x)) return SC_ERR_ALIGN;
+    if (Cout > 1 && !aligned16(y)) return SC_ERR_ALIGN;
+    const size_t ybytes = (size_t)ny * sizeof(float);
+    if (overlaps(y, ybytes, x, (size_t)nx * sizeof(float)) ||
+        overlaps(y, ybytes, w, (size_t)nw * sizeof(float)) ||
+        overlaps(y, ybytes, b, b ? (size_t)Cout * sizeof(float) : 0))
+        return SC_ERR_ALIAS;
+    return SC_OK;
+}
 
 cudaError_t launch_conv_nhwc(const ConvArgs &a, cudaStream_t st)
 {
@@ -131,6 +164,7 @@ cudaError_t workspace_alloc(void **p, size_t bytes, cudaStream_t st)
     cudaMemPool_t pool = nullptr;
     const cudaError_t e = workspace_pool(&pool);
     if (e != cudaSuccess) return e;
+    g_workspace_allocs.fetch_add(1, std::memory_order_relaxed);
     return cudaMallocFromPoolAsync(p, bytes, pool, st);
 }
 
@@ -166,27 +200,9 @@ extern "C" {
 int conv2d_fwd(const float *x, const float *w, const float *b, float *y, int N, int H, int W,
                int Cin, int Cout, int R, int S, int layout, int act, sc_stream_t stream)
 {
-    if (!x || !w || !y) return SC_ERR_NULL;
-    const long long nx = checked_count({N, H, W, Cin});
-    const long long ny = checked_count({N, H, W, Cout});
-    const long long nw = checked_count({Cout, Cin, R, S});
-    if (nx < 0 || ny < 0 || nw < 0) return SC_ERR_SHAPE;
-    if (H > (1 << 30) || W > (1 << 30)) return SC_ERR_SHAPE;
-    if ((R & 1) == 0 || (S & 1) == 0 || R > 7 || S > 7) return SC_ERR_UNSUPPORTED;
-    if (layout != SC_NCHW && layout != SC_NHWC) return SC_ERR_UNSUPPORTED;
-    if (act != SC_ACT_NONE && act != SC_ACT_RELU) return SC_ERR_UNSUPPORTED;
-    if (Cin == 1) {
-        if (Cout != 1 && (Cout % 4) != 0) return SC_ERR_UNSUPPORTED;
-    } else {
-        if ((Cin % 4) != 0 || (Cout % 4) != 0) return SC_ERR_UNSUPPORTED;
-    }
-    if (Cin > 1 && !aligned16(x)) return SC_ERR_ALIGN;
-    if (Cout > 1 && !aligned16(y)) return SC_ERR_ALIGN;
-    const size_t ybytes = (size_t)ny * sizeof(float);
-    if (overlaps(y, ybytes, x, (size_t)nx * sizeof(float)) ||
-        overlaps(y, ybytes, w, (size_t)nw * sizeof(float)) ||
-        overlaps(y, ybytes, b, b ? (size_t)Cout * sizeof(float) : 0))
-        return SC_ERR_ALIAS;
+    const int chk = sc::check_conv_args(x, w, b, y, N, H, W, Cin, Cout, R, S, layout, act);
+    if (chk != SC_OK) return chk;
+    const long long nx = (long long)N * H * W * Cin, ny = (long long)N * H * W * Cout;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     sc::ConvArgs a{x, w, b, y, N, H, W, Cin, Cout, R, S, act};
@@ -409,6 +425,8 @@ int sc_test_conv_candidate(const float *x, const float *w, const float *b, float
     }
     return e == cudaSuccess ? SC_OK : cuda_fail(e);
 }
+
+long long sc_test_workspace_allocs(void) { return g_workspace_allocs.load(std::memory_order_relaxed); }
 
 int sc_release_workspace(void)
 {

@@ -139,6 +139,13 @@ cudaError_t resident_ctas(KernelCache &c, int dev, K kernel, int threads, int sm
 cudaError_t workspace_alloc(void **p, size_t bytes, cudaStream_t st);
 cudaError_t workspace_free(void *p, cudaStream_t st);
 
+// conv2d_fwd's argument checks (api.cu), shared by every entry point with
+// its contract: SC_OK when the call may launch, else the status to return.
+int check_conv_args(const float *x, const float *w, const float *b, const float *y, int N, int H, int W, int Cin,
+                    int Cout, int R, int S, int layout, int act);
+// Records e for sc_last_cuda_error (per host thread) and returns SC_ERR_CUDA.
+int record_cuda_error(cudaError_t e);
+
 // Device address of the current device's status word (api.cu), or nullptr.
 int *device_status_ptr();
 

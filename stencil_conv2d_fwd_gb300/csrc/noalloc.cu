@@ -2,7 +2,6 @@
 // allocation.  conv2d_fwd with SC_NCHW repacks through a temporary buffer it
 // allocates on the stream; this entry point uses a fixed array in the
 // library's own device memory instead.  Contract: include/stencilconv.h.
-#include <cstdint>
 #include <mutex>
 
 #include "../../include/stencilconv.h"
@@ -38,27 +37,7 @@ float *scratch_on_current_device(cudaError_t *err)
     return addr[dev];
 }
 
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-bool overlaps(const void *a, size_t abytes, const void *b, size_t bbytes)
-{
-    if (!a || !b || abytes == 0 || bbytes == 0) return false;
-    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
-    return a0 < b0 + bbytes && b0 < a0 + abytes;
-}
-
-long long count4(int a, int b, int c, int d)
-{
-    const int v[4] = {a, b, c, d};
-    long long n = 1;
-    for (int x : v) {
-        if (x < 1 || n > (1LL << 62) / x) return -1;
-        n *= x;
-    }
-    return n;
-}
-
-int fail(cudaError_t) { return SC_ERR_CUDA; }
+int fail(cudaError_t e) { return sc::record_cuda_error(e); }
 
 }  // namespace
 
@@ -66,23 +45,9 @@ extern "C" int conv2d_fwd_nchw_noalloc(const float *x, const float *w, const flo
                                        int N, int H, int W, int Cin, int Cout, int R, int S, int act,
                                        sc_stream_t stream)
 {
-    if (!x || !w || !y) return SC_ERR_NULL;
-    const long long nx = count4(N, H, W, Cin), ny = count4(N, H, W, Cout), nw = count4(Cout, Cin, R, S);
-    if (nx < 0 || ny < 0 || nw < 0 || H > (1 << 30) || W > (1 << 30)) return SC_ERR_SHAPE;
-    if ((R & 1) == 0 || (S & 1) == 0 || R > 7 || S > 7) return SC_ERR_UNSUPPORTED;
-    if (act != SC_ACT_NONE && act != SC_ACT_RELU) return SC_ERR_UNSUPPORTED;
-    if (Cin == 1) {
-        if (Cout != 1 && (Cout % 4) != 0) return SC_ERR_UNSUPPORTED;
-    } else if ((Cin % 4) != 0 || (Cout % 4) != 0) {
-        return SC_ERR_UNSUPPORTED;
-    }
-    if (Cin > 1 && !aligned16(x)) return SC_ERR_ALIGN;
-    if (Cout > 1 && !aligned16(y)) return SC_ERR_ALIGN;
-    const size_t ybytes = (size_t)ny * sizeof(float);
-    if (overlaps(y, ybytes, x, (size_t)nx * sizeof(float)) ||
-        overlaps(y, ybytes, w, (size_t)nw * sizeof(float)) ||
-        overlaps(y, ybytes, b, b ? (size_t)Cout * sizeof(float) : 0))
-        return SC_ERR_ALIAS;
+    const int chk = sc::check_conv_args(x, w, b, y, N, H, W, Cin, Cout, R, S, SC_NCHW, act);
+    if (chk != SC_OK) return chk;
+    const long long nx = (long long)N * H * W * Cin, ny = (long long)N * H * W * Cout;
 
     // Scratch: NHWC x (when Cin > 1), then NHWC y (when Cout > 1), each
     // starting on a 256-byte boundary.

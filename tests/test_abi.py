@@ -81,6 +81,32 @@ def test_conv_argument_errors(args, expect):
     assert rc == expect, sc.sc_status_string(rc)
 
 
+@pytest.mark.parametrize("args,expect", [
+    (dict(x=None), sc.SC_ERR_NULL),
+    (dict(y=None), sc.SC_ERR_NULL),
+    (dict(N=0), sc.SC_ERR_SHAPE),
+    (dict(W=-3), sc.SC_ERR_SHAPE),
+    (dict(R=2), sc.SC_ERR_UNSUPPORTED),
+    (dict(R=9, S=9), sc.SC_ERR_UNSUPPORTED),
+    (dict(act=3), sc.SC_ERR_UNSUPPORTED),
+    (dict(Cin=6), sc.SC_ERR_UNSUPPORTED),
+    (dict(Cin=1, Cout=6), sc.SC_ERR_UNSUPPORTED),
+    (dict(x=A16 + 4), sc.SC_ERR_ALIGN),
+    (dict(y=B16 + 8), sc.SC_ERR_ALIGN),
+    (dict(y=A16 + 64), sc.SC_ERR_ALIAS),
+    (dict(b=B16), sc.SC_ERR_ALIAS),
+])
+def test_noalloc_entry_point_rejects_what_conv2d_fwd_rejects(args, expect):
+    """conv2d_fwd_nchw_noalloc promises conv2d_fwd's (NCHW) argument rules and status codes."""
+    a = dict(x=A16, w=1 << 28, b=None, y=B16, N=1, H=8, W=8, Cin=4, Cout=4, R=3, S=3, act=0)
+    a.update(args)
+    rc_ref = sc.conv2d_fwd(a["x"], a["w"], a["b"], a["y"], a["N"], a["H"], a["W"], a["Cin"], a["Cout"],
+                           a["R"], a["S"], sc.SC_NCHW, a["act"], stream=0)
+    rc = sc.conv2d_fwd_nchw_noalloc(a["x"], a["w"], a["b"], a["y"], a["N"], a["H"], a["W"], a["Cin"],
+                                    a["Cout"], a["R"], a["S"], a["act"], stream=0)
+    assert rc == rc_ref == expect, sc.sc_status_string(rc)
+
+
 def test_size_overflow_is_a_shape_error():
     rc = sc.conv2d_fwd(A16, 1 << 28, None, B16, 1 << 30, 1 << 30, 1 << 30, 4, 4, 3, 3, 1, 0, stream=0)
     assert rc == sc.SC_ERR_SHAPE

@@ -2,10 +2,12 @@
 allocate device memory during the call (a process that reserved the GPU's
 memory up front, a real-time frame loop that cannot risk an allocation).
 
-It must give what conv2d_fwd gives with layout NCHW, within the fp32 parity
-tolerance |y - y_ref| <= 1e-5 * (sum |x * w| + |b|), on two calls in a row:
-the second call starts with the first call's data still in the shared
-scratch array.  This file is collected last on purpose.
+It must match the fp64 oracle within the fp32 parity tolerance
+|y - y_ref| <= 1e-5 * (sum |x * w| + |b|) on two calls in a row (the second
+call starts with the first call's data still in the shared scratch array),
+take no buffer from the library's memory pool, and accept a problem that
+needs exactly the whole scratch array.  This file is collected last on
+purpose.
 """
 import numpy as np
 import pytest
@@ -36,22 +38,44 @@ def _run(fn, c, dev, with_layout):
     return yd.cpu().numpy().reshape(N, L.cout, H, W)
 
 
-def test_noalloc_matches_conv2d_fwd_on_two_calls_in_a_row(oracle_mod, cuda_dev, sc):
-    cases = [S.conv_case(901, 2, 16, 32, 37, 53, 3, 3, act=1),   # larger: fills more scratch
-             S.conv_case(902, 1, 8, 12, 19, 23, 5, 5, act=0),    # smaller: stale data beyond its end
-             S.conv_case(903, 1, 1, 16, 21, 33, 5, 5, act=1)]    # Cin = 1: only the output repack
-    for c in cases:
-        L = c.layers[0]
-        _, a = oracle_mod.conv2d_nchw(c.x, L.w, L.b, L.act)
-        ref = _run(sc.conv2d_fwd, c, cuda_dev, True)
-        for _ in range(2):
-            got = _run(sc.conv2d_fwd_nchw_noalloc, c, cuda_dev, False)
-            assert (np.abs(got.astype(np.float64) - ref) <= CONV_RTOL * a).all()
+def _scratch_floats(N, H, W, Cin, Cout):
+    """Scratch a call needs: NHWC x rounded up to 64 floats, then NHWC y."""
+    nx = N * H * W * Cin if Cin > 1 else 0
+    return (nx + 63) // 64 * 64 + (N * H * W * Cout if Cout > 1 else 0)
+
+
+CASES = [
+    (901, 2, 16, 32, 37, 53, 3, 1),   # larger: fills more scratch
+    (902, 1, 8, 12, 19, 23, 5, 0),    # smaller: stale data beyond its end
+    (903, 1, 1, 16, 21, 33, 5, 1),    # Cin = 1: only the output repack
+    (904, 1, 4, 4, 1024, 1024, 3, 1),  # needs exactly the whole scratch array
+]
+
+
+def test_exact_limit_case_fills_the_scratch():
+    _, N, Cin, Cout, H, W, _, _ = CASES[3]
+    assert _scratch_floats(N, H, W, Cin, Cout) == sc.SC_NOALLOC_SCRATCH_FLOATS
+
+
+@pytest.mark.parametrize("case", CASES, ids=[str(c[0]) for c in CASES])
+def test_noalloc_matches_the_oracle_on_two_calls_in_a_row(oracle_mod, cuda_dev, sc, case):
+    seed, N, Cin, Cout, H, W, K, act = case
+    c = S.conv_case(seed, N, Cin, Cout, H, W, K, K, act=act)
+    L = c.layers[0]
+    y_ref, a = oracle_mod.conv2d_nchw(c.x, L.w, L.b, L.act)
+    ref = _run(sc.conv2d_fwd, c, cuda_dev, True)
+    allocs = sc.sc_test_workspace_allocs()
+    for _ in range(2):
+        got = _run(sc.conv2d_fwd_nchw_noalloc, c, cuda_dev, False).astype(np.float64)
+        assert (np.abs(got - y_ref) <= CONV_RTOL * a).all()
+        # and the same as the allocating entry point, which runs the same kernels
+        assert (np.abs(got - ref) <= CONV_RTOL * a).all()
+    assert sc.sc_test_workspace_allocs() == allocs, "the no-allocation entry point took a pool buffer"
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(cuda_dev, sc):
-    N, C, H, W = 1, 64, 256, 300          # 2 * 64*256*300 floats > 8 Mi
-    assert 2 * N * C * H * W > sc.SC_NOALLOC_SCRATCH_FLOATS
+    N, C, H, W = 1, 4, 1024, 1025        # one column more than the exact-limit case
+    assert _scratch_floats(N, H, W, C, C) > sc.SC_NOALLOC_SCRATCH_FLOATS
     x = torch.zeros(N * C * H * W, device=cuda_dev)
     w = torch.zeros(C * C * 9, device=cuda_dev)
     y = torch.full((N * C * H * W,), 5.0, device=cuda_dev)
