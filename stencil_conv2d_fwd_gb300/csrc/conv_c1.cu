@@ -517,15 +517,6 @@ __global__ void __launch_bounds__(32 * kC1TileWarps, kC1TileCtas)
     const uint32_t obase = (raw_u + 1023) & ~1023u;
     float *tile = reinterpret_cast<float *>(c1t_raw + (obase - raw_u) + kC1TileWarps * kC1TileOutBuf);
 
-    for (int e = tid; e < K * K * CO; e += 32 * kC1TileWarps) {
-        const int col = e % CO, tap = e / CO;
-        const int r = tap / K - (K - R) / 2, s = tap % K - (K - S) / 2;
-        const int co = co0 + col;
-        float v = 0.f;
-        if (r >= 0 && r < R && s >= 0 && s < S && co < Cout) v = w[((long long)co * R + r) * S + s];
-        ws[e] = v;
-    }
-    for (int e = tid; e < CO; e += 32 * kC1TileWarps) bs[e] = (bias && co0 + e < Cout) ? bias[co0 + e] : 0.f;
     // staged column c of row r is image pixel (y0 - HALO + r, tx0 - 4 + c);
     // 16-byte pieces are wholly inside or outside the image (W % 4 == 0)
     // two copy groups: the K rows of the first output row, then the rest,
@@ -542,8 +533,19 @@ __global__ void __launch_bounds__(32 * kC1TileWarps, kC1TileCtas)
         }
         cp_async_commit();
     };
+    // the band's copies first, so that their latency overlaps the filter
+    // and bias loads below
     stage_rows(0, K);
     stage_rows(K, nin);
+    for (int e = tid; e < K * K * CO; e += 32 * kC1TileWarps) {
+        const int col = e % CO, tap = e / CO;
+        const int r = tap / K - (K - R) / 2, s = tap % K - (K - S) / 2;
+        const int co = co0 + col;
+        float v = 0.f;
+        if (r >= 0 && r < R && s >= 0 && s < S && co < Cout) v = w[((long long)co * R + r) * S + s];
+        ws[e] = v;
+    }
+    for (int e = tid; e < CO; e += 32 * kC1TileWarps) bs[e] = (bias && co0 + e < Cout) ? bias[co0 + e] : 0.f;
     cp_async_wait<1>();
     __syncthreads();
 
@@ -640,7 +642,9 @@ __global__ void __launch_bounds__(32 * kC1TileWarps, kC1TileCtas)
             bulk_commit();
         }
     }
-    if (lane == 0) bulk_wait_all();   // every store has written global memory
+    // the buffers must outlive the stores' reads of them; the stores' writes
+    // to global memory complete before the grid does
+    if (lane == 0) bulk_wait_read<0>();
 }
 
 template <int K>
@@ -738,9 +742,84 @@ static cudaError_t launch_c1_k(const ConvArgs &a, cudaStream_t st)
     return launch_c1_cfg<K, 8, 4>(a, st);
 }
 
+// Small images with one output channel (a few thousand pixels): the row
+// sweep above would leave most SMs idle and walk its rows one after another,
+// each behind a load.  Here each thread computes 4 horizontally adjacent
+// output pixels of one row on its own and issues all its loads (the K x K
+// filter, the bias and K rows of 4 + K - 1 pixels, zero outside the image)
+// at once, so a launch costs about one load latency after the launch
+// itself.  FMA order as in the kernels above: bias, then the taps row by
+// row.
+constexpr int kC1SmallThreads = 64;
+constexpr long long kC1SmallPixels = 1LL << 16;   // N * H * W up to which it is used
+
+template <int K>
+__global__ void __launch_bounds__(kC1SmallThreads)
+    conv_c1_small_kernel(const float *__restrict__ x, const float *__restrict__ w, const float *__restrict__ bias,
+                         float *__restrict__ y, int N, int H, int W, int R, int S, int act)
+{
+    constexpr int HALO = K / 2, WIN = 4 + K - 1;
+    const int qw = (W + 3) / 4;
+    const long long t = (long long)blockIdx.x * kC1SmallThreads + threadIdx.x;
+    if (t >= (long long)N * H * qw) return;
+    const int x0 = 4 * (int)(t % qw);
+    const long long row = t / qw;   // n * H + oy
+    const int oy = (int)(row % H);
+    const float *xn = x + (row - oy) * W;
+    float wv[K * K];
+#pragma unroll
+    for (int ky = 0; ky < K; ++ky)
+#pragma unroll
+        for (int kx = 0; kx < K; ++kx) {
+            const int r = ky - (K - R) / 2, s = kx - (K - S) / 2;
+            wv[ky * K + kx] = (r >= 0 && r < R && s >= 0 && s < S) ? __ldg(w + r * S + s) : 0.f;
+        }
+    float win[K][WIN];
+#pragma unroll
+    for (int ky = 0; ky < K; ++ky) {
+        const int iy = oy - HALO + ky;
+#pragma unroll
+        for (int c = 0; c < WIN; ++c) {
+            const int ix = x0 - HALO + c;
+            win[ky][c] = (iy >= 0 && iy < H && ix >= 0 && ix < W) ? __ldg(xn + (long long)iy * W + ix) : 0.f;
+        }
+    }
+    const float b = bias ? __ldg(bias) : 0.f;
+    float acc[4] = {b, b, b, b};
+#pragma unroll
+    for (int ky = 0; ky < K; ++ky)
+#pragma unroll
+        for (int kx = 0; kx < K; ++kx)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[j] = fmaf(wv[ky * K + kx], win[ky][j + kx], acc[j]);
+    float *yr = y + row * W;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        if (x0 + j < W) yr[x0 + j] = relu_if(acc[j], act);
+}
+
+template <int K>
+static cudaError_t launch_c1_small(const ConvArgs &a, cudaStream_t st)
+{
+    const long long threads = (long long)a.N * a.H * ((a.W + 3) / 4);
+    const long long blocks = (threads + kC1SmallThreads - 1) / kC1SmallThreads;
+    conv_c1_small_kernel<K><<<(unsigned)blocks, kC1SmallThreads, 0, st>>>(a.x, a.w, a.b, a.y, a.N, a.H, a.W, a.R,
+                                                                         a.S, a.act);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_conv_c1(const ConvArgs &a, cudaStream_t st)
 {
     const int K = a.R > a.S ? a.R : a.S;
+    if (a.Cout == 1 && (long long)a.N * a.H * a.W <= kC1SmallPixels) {
+        switch (K) {
+        case 1: return launch_c1_small<1>(a, st);
+        case 3: return launch_c1_small<3>(a, st);
+        case 5: return launch_c1_small<5>(a, st);
+        case 7: return launch_c1_small<7>(a, st);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     switch (K) {
     case 1: return launch_c1_k<1>(a, st);
     case 3: return launch_c1_k<3>(a, st);
