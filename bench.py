@@ -371,11 +371,37 @@ def run_ours(args, rank, world, local):
         if not args.no_per_config:
             result["cpu_baseline"]["per_config"] = oracle_per_config(S)
 
+    if "per_config" in result:
+        # compact per-workload summary, last in the line: [ms mean, roofline frac]
+        result["per_config_summary"] = per_config_summary(result["per_config"])
+
     if world > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
     if rank == 0:
         print(json.dumps(result))
+
+
+def per_config_summary(pc):
+    """{short name: [ms mean, roofline fraction]} of every timed entry of
+    per_config (plus the graph per-launch time and the launch floor in us
+    for workloads 1 and 2)."""
+    tags = (("replayed as a CUDA graph", "graph"), ("split-TF32 tensor cores", "x3 net"),
+            ("tcgen05 split TF32", "x3"), ("tcgen05 TF32", "tf32"), ("tcgen05 BF16", "bf16"))
+    out = {}
+    for name, e in pc.items():
+        if name.startswith("_") or "ms_mean" not in e:
+            continue
+        short = name.split(":")[0] if ":" in name else name.split(" (")[0]
+        for pat, tag in tags:
+            if pat in name:
+                short += " " + tag
+                break
+        v = [e["ms_mean"], e.get("roofline_frac")]
+        if "graph_ms_per_launch" in e:
+            v += [e["graph_ms_per_launch"], e.get("launch_floor_us")]
+        out[short] = v
+    return out
 
 
 class L2Flush:
@@ -399,7 +425,12 @@ class L2Flush:
         self.rd.sum()
 
 
-def time_events(fn, stream, flush, reps, warm=3):
+def time_events(fn, stream, flush, reps=40, warm=3):
+    """(mean, min, median) of `reps` timed calls in ms, `flush` before each.
+
+    CUDA-event timestamps on this GPU advance in steps of about 1.02 us, so a
+    median of a few tens of microseconds sits on that grid; the mean over
+    many calls does not, and is the figure the fractions are taken from."""
     import torch
     for _ in range(warm):
         flush(0.0)
@@ -413,7 +444,7 @@ def time_events(fn, stream, flush, reps, warm=3):
         e1.record(stream)
         torch.cuda.synchronize()
         ts.append(e0.elapsed_time(e1))
-    return statistics.median(ts), min(ts)
+    return sum(ts) / len(ts), min(ts), statistics.median(ts)
 
 
 def time_graph(fn, stream, launches=100, reps=5):
@@ -461,14 +492,14 @@ def per_config(sc, S, dev, stream, flush, fp32_tflops, hbm_gbs, hbm_src):
                                s if s is not None else stream)
             if rc != 0:
                 raise RuntimeError(sc.sc_status_string(rc))
-        med, mn = time_events(call, stream, flush, reps=20)
+        med, mn, mdn = time_events(call, stream, flush)
         names = sc.sc_autotune_candidates(L.cin, L.cout, L.r, L.s)
         choice = sc.sc_autotune_lookup(n, h, w, L.cin, L.cout, L.r, L.s, L.act, True)
         flops = conv_flops(n, h, w, L)
         byts = 4 * (n * h * w * (L.cin + L.cout) + L.w.size + L.b.size)
         t_roof = max(flops / (fp32_tflops * 1e12), byts / (hbm_gbs * 1e9))
         bound = "alu" if flops / (fp32_tflops * 1e12) >= byts / (hbm_gbs * 1e9) else "hbm"
-        e = {"ms_median": round(med, 5), "ms_min": round(mn, 5),
+        e = {"ms_mean": round(med, 5), "ms_median": round(mdn, 5), "ms_min": round(mn, 5),
              "gflops": round(flops / (med * 1e-3) / 1e9, 2),
              "mpixel_per_s": round(n * h * w / (med * 1e-3) / 1e6, 2),
              "roofline_bound": bound, "roofline_us": round(t_roof * 1e6, 3),
@@ -478,11 +509,23 @@ def per_config(sc, S, dev, stream, flush, fp32_tflops, hbm_gbs, hbm_src):
             per = time_graph(call, stream)
             e["graph_ms_per_launch"] = round(per, 5)
             e["graph_roofline_frac"] = round(t_roof / (per * 1e-3), 4)
+            e["launch_floor_us"] = floor_us
+            e["graph_per_launch_vs_floor"] = round(per * 1e3 / floor_us, 3)
         if warm:   # back to back without the L2 flush (inputs partly L2-resident)
-            wmed, _ = time_events(call, stream, no_flush, reps=20)
-            e["ms_median_warm_l2"] = round(wmed, 5)
+            wmed, _, _ = time_events(call, stream, no_flush)
+            e["ms_mean_warm_l2"] = round(wmed, 5)
         out[name] = e
         return yd
+
+    # the launch floor: a kernel that does nothing (one CTA of 128 threads per
+    # SM), replayed back to back from the same CUDA-graph harness
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+
+    def empty(s=None):
+        sc.check(sc.sc_empty_kernel(n_sm, 128, s if s is not None else stream))
+    floor_us = round(time_graph(empty, stream) * 1e3, 3)
+    out["launch_floor"] = {"us_per_launch": floor_us,
+                           "note": f"empty kernel, {n_sm} CTAs x 128 threads, 100 launches in one CUDA graph"}
 
     c1 = S.config(1)
     conv_entry("1: 64x64 1->1 3x3", 1, 64, 64, c1.layers[0], c1.x[0, 0], graph=True)
@@ -496,6 +539,24 @@ def per_config(sc, S, dev, stream, flush, fp32_tflops, hbm_gbs, hbm_src):
         prev = yd.view(720, 1280, L.cout).cpu().numpy()
     c4 = S.config(4)
     conv_entry("4: N=32 56x56 64->64 3x3", 32, 56, 56, c4.layers[0], c4.x.transpose(0, 2, 3, 1), warm=True)
+
+    # S1, the activation repack NCHW -> NHWC at workload 4's size (what
+    # conv2d_fwd with SC_NCHW runs before the convolution): pure bandwidth
+    rp_src = torch.from_numpy(np.ascontiguousarray(c4.x)).to(dev)
+    rp_dst = torch.empty_like(rp_src)
+    n4, c4c, h4, w4 = c4.x.shape
+
+    def repack(s=None):
+        sc.check(sc.sc_repack(rp_src, rp_dst, n4, c4c, h4, w4, sc.SC_NCHW, sc.SC_NHWC,
+                              s if s is not None else stream))
+    med, mn, mdn = time_events(repack, stream, flush)
+    byts = 2 * 4 * rp_src.numel()
+    out["S1: repack NCHW->NHWC N=32 64x56x56"] = {
+        "ms_mean": round(med, 5), "ms_median": round(mdn, 5), "ms_min": round(mn, 5),
+        "gbytes_per_s": round(byts / (med * 1e-3) / 1e9, 1),
+        "roofline_bound": "hbm", "roofline_us": round(byts / (hbm_gbs * 1e9) * 1e6, 3),
+        "roofline_frac": round(byts / (hbm_gbs * 1e9) / (med * 1e-3), 4),
+        "note": "read and write of the 25.7 MB activation once each"}
 
     # the FFMA net (the headline pass) captured once into a CUDA graph and
     # replayed: the same three kernels without the host's launch gaps between
@@ -520,9 +581,9 @@ def per_config(sc, S, dev, stream, flush, fp32_tflops, hbm_gbs, hbm_src):
         net_calls(side)
     torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
-    gmed, gmn = time_events(lambda: graph.replay(), stream, flush, reps=20)
+    gmed, gmn, gmdn = time_events(lambda: graph.replay(), stream, flush)
     out["3: 3-layer net replayed as a CUDA graph"] = {
-        "ms_median": round(gmed, 5), "ms_min": round(gmn, 5),
+        "ms_mean": round(gmed, 5), "ms_median": round(gmdn, 5), "ms_min": round(gmn, 5),
         "gflops": round(sum(conv_flops(1, 720, 1280, L) for L in c3.layers) / (gmed * 1e-3) / 1e9, 2),
         "note": "the headline pass's three FFMA kernels without host launch gaps"}
 
@@ -550,12 +611,12 @@ def per_config(sc, S, dev, stream, flush, fp32_tflops, hbm_gbs, hbm_src):
                            s if s is not None else stream)
                 if rc != 0:
                     raise RuntimeError(sc.sc_status_string(rc))
-            med, mn = time_events(call_tc, stream, flush, reps=20)
+            med, mn, mdn = time_events(call_tc, stream, flush)
             flops = conv_flops(wl.n, wl.h, wl.w, L)
             byts = 4 * (wl.n * wl.h * wl.w * (L.cin + L.cout) + L.w.size + L.b.size)
             t_c, t_m = work * flops / (tf32_tflops * 1e12), byts / (hbm_gbs * 1e9)
             out[f"{cname} ({vname})"] = {
-                "ms_median": round(med, 5), "ms_min": round(mn, 5),
+                "ms_mean": round(med, 5), "ms_median": round(mdn, 5), "ms_min": round(mn, 5),
                 "gflops": round(flops / (med * 1e-3) / 1e9, 2),
                 "mpixel_per_s": round(wl.n * wl.h * wl.w / (med * 1e-3) / 1e6, 2),
                 "roofline_bound": "tensor" if t_c >= t_m else "hbm",
@@ -584,11 +645,11 @@ def per_config(sc, S, dev, stream, flush, fp32_tflops, hbm_gbs, hbm_src):
                                        sc.SC_BF16, s if s is not None else stream)
             if rc != 0:
                 raise RuntimeError(sc.sc_status_string(rc))
-        med, mn = time_events(call_bf, stream, flush, reps=20)
+        med, mn, mdn = time_events(call_bf, stream, flush)
         flops = conv_flops(wl.n, wl.h, wl.w, L)
         byts = 2 * wl.n * wl.h * wl.w * (L.cin + L.cout) + 4 * (L.w.size + L.b.size)
         t_c, t_m = flops / (bf16_tflops * 1e12), byts / (hbm_gbs * 1e9)
-        out[name] = {"ms_median": round(med, 5), "ms_min": round(mn, 5),
+        out[name] = {"ms_mean": round(med, 5), "ms_median": round(mdn, 5), "ms_min": round(mn, 5),
                      "gflops": round(flops / (med * 1e-3) / 1e9, 2),
                      "mpixel_per_s": round(wl.n * wl.h * wl.w / (med * 1e-3) / 1e6, 2),
                      "roofline_bound": "tensor" if t_c >= t_m else "hbm",
@@ -612,12 +673,12 @@ def per_config(sc, S, dev, stream, flush, fp32_tflops, hbm_gbs, hbm_src):
                                      L2.act, L3.act, s if s is not None else stream)
         if rc != 0:
             raise RuntimeError(sc.sc_status_string(rc))
-    med, mn = time_events(call_fused, stream, flush, reps=20)
+    med, mn, mdn = time_events(call_fused, stream, flush)
     flops = conv_flops(wl.n, wl.h, wl.w, L2) + conv_flops(wl.n, wl.h, wl.w, L3)
     byts = 4 * (wl.n * wl.h * wl.w * (L2.cin + L3.cout) + L2.w.size + L2.b.size + L3.w.size + L3.b.size)
     t_c, t_m = flops / (tf32_tflops * 1e12), byts / (hbm_gbs * 1e9)
     out["3-L2+3-L3 fused (tcgen05 TF32)"] = {
-        "ms_median": round(med, 5), "ms_min": round(mn, 5),
+        "ms_mean": round(med, 5), "ms_median": round(mdn, 5), "ms_min": round(mn, 5),
         "gflops": round(flops / (med * 1e-3) / 1e9, 2),
         "mpixel_per_s": round(wl.n * wl.h * wl.w / (med * 1e-3) / 1e6, 2),
         "roofline_bound": "tensor" if t_c >= t_m else "hbm",
@@ -646,10 +707,10 @@ def per_config(sc, S, dev, stream, flush, fp32_tflops, hbm_gbs, hbm_src):
                    sc.conv2d_fwd_tc_x3(a2, *wds[2], a3, wl.n, wl.h, wl.w, L3.cin, L3.cout, L3.r, L3.s, L3.act, st_)):
             if rc != 0:
                 raise RuntimeError(sc.sc_status_string(rc))
-    med, mn = time_events(call_net_x3, stream, flush, reps=20)
+    med, mn, mdn = time_events(call_net_x3, stream, flush)
     flops = sum(conv_flops(wl.n, wl.h, wl.w, L) for L in (L1, L2, L3))
     out["3: 3-layer net, layers 2 and 3 on split-TF32 tensor cores"] = {
-        "ms_median": round(med, 5), "ms_min": round(mn, 5),
+        "ms_mean": round(med, 5), "ms_median": round(mdn, 5), "ms_min": round(mn, 5),
         "gflops": round(flops / (med * 1e-3) / 1e9, 2),
         "mpixel_per_s": round(n_px / (med * 1e-3) / 1e6, 2),
         "tolerance": "1e-5 * sum|x*w| per layer (the fp32 bound of every layer)",
@@ -663,17 +724,17 @@ def per_config(sc, S, dev, stream, flush, fp32_tflops, hbm_gbs, hbm_src):
         rc = sc.stencil_pipeline_fwd(ind, outd, c5.h, c5.w, stream)
         if rc != 0:
             raise RuntimeError(sc.sc_status_string(rc))
-    med, mn = time_events(pipe, stream, flush, reps=20)
-    wmed, _ = time_events(pipe, stream, no_flush, reps=20)
+    med, mn, mdn = time_events(pipe, stream, flush)
+    wmed, _, _ = time_events(pipe, stream, no_flush)
     byts = 8 * c5.h * c5.w
     t_roof = byts / (hbm_gbs * 1e9)
     out["5: 4096x4096 fused blur/unsharp"] = {
-        "ms_median": round(med, 5), "ms_min": round(mn, 5),
+        "ms_mean": round(med, 5), "ms_median": round(mdn, 5), "ms_min": round(mn, 5),
         "mpixel_per_s": round(c5.h * c5.w / (med * 1e-3) / 1e6, 2),
         "gbytes_per_s": round(byts / (med * 1e-3) / 1e9, 1),
         "roofline_bound": "hbm", "roofline_us": round(t_roof * 1e6, 3),
         "roofline_frac": round(t_roof / (med * 1e-3), 4),
-        "ms_median_warm_l2": round(wmed, 5)}
+        "ms_mean_warm_l2": round(wmed, 5)}
     out["_peaks"] = {"fp32_tflops": round(fp32_tflops, 2), "hbm_gbs": hbm_gbs, "hbm_source": hbm_src,
                      "fp32_source": "nominal: SMs x 128 FP32 lanes x 2 x max SM clock"}
     return out

@@ -221,6 +221,16 @@ int sc_last_cuda_error(void);
  */
 int sc_measure_ffma_peak(float *sink, int blocks, int iters, sc_stream_t stream);
 
+/*
+ * sc_empty_kernel: measurement helper, not part of the operation.  Launches
+ * a kernel of `blocks` CTAs of `threads` threads that does nothing, on
+ * `stream`; a run of such launches (e.g. replayed from a CUDA graph) gives
+ * the cost of one launch, the floor under any kernel of the library.
+ * Returns SC_OK, SC_ERR_SHAPE for blocks outside [1, 2^24] or threads
+ * outside [1, 1024], or SC_ERR_CUDA.
+ */
+int sc_empty_kernel(int blocks, int threads, sc_stream_t stream);
+
 /* sc_version: library version as 10000*major + 100*minor + patch. */
 int sc_version(void);
 

@@ -49,6 +49,7 @@ SIGNATURES = {
     "sc_last_cuda_error": (_I, []),
     "sc_measure_ffma_peak": (_I, [_P, _I, _I, _P]),
     "sc_version": (_I, []),
+    "sc_empty_kernel": (_I, [_I, _I, _P]),
     "sc_release_workspace": (_I, []),
     "sc_set_autotune": (_I, [_I]),
     "sc_autotune_lookup": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _I]),
@@ -209,6 +210,11 @@ def conv2d_fwd_nchw_noalloc(x, w, b, y, N, H, W, Cin, Cout, R, S, act=SC_ACT_NON
     """NCHW conv2d_fwd that allocates no device memory (see the header)."""
     return load().conv2d_fwd_nchw_noalloc(_ptr(x), _ptr(w), _ptr(b), _ptr(y), N, H, W, Cin, Cout, R, S,
                                           act, _stream(stream))
+
+
+def sc_empty_kernel(blocks, threads, stream=None) -> int:
+    """Launch a kernel that does nothing (launch-cost probe; see the header)."""
+    return load().sc_empty_kernel(blocks, threads, _stream(stream))
 
 
 def sc_test_workspace_allocs() -> int:

@@ -405,6 +405,13 @@ int sc_measure_ffma_peak(float *sink, int blocks, int iters, sc_stream_t stream)
     return e == cudaSuccess ? SC_OK : cuda_fail(e);
 }
 
+int sc_empty_kernel(int blocks, int threads, sc_stream_t stream)
+{
+    if (blocks < 1 || blocks > (1 << 24) || threads < 1 || threads > 1024) return SC_ERR_SHAPE;
+    cudaError_t e = sc::launch_empty(blocks, threads, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SC_OK : cuda_fail(e);
+}
+
 int sc_version(void) { return 100; }
 
 int sc_test_conv_candidate(const float *x, const float *w, const float *b, float *y, int N, int H, int W, int Cin,

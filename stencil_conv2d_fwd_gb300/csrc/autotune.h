@@ -24,9 +24,18 @@ cudaError_t k3_tma_f4_w5_h4(const ConvArgs &a, cudaStream_t st);
 cudaError_t k3_tma_f4_w5_h8_pc(const ConvArgs &a, cudaStream_t st);
 cudaError_t k3_tma_f4_w3_h4_pc(const ConvArgs &a, cudaStream_t st);
 cudaError_t k3_tma_f4_w5_h8r2(const ConvArgs &a, cudaStream_t st);
+cudaError_t k3_tma_f4_w5_h8(const ConvArgs &a, cudaStream_t st);
+cudaError_t k3_tma_f4_w5_h8_s4(const ConvArgs &a, cudaStream_t st);
 cudaError_t k3_tma_f8_w5_h4(const ConvArgs &a, cudaStream_t st);
+// The narrow-output kernel (conv_narrow_k3.cu): 32 -> 4 channels, 8 x 160
+// pixel tiles; "s4": four stages of 8 channels, "c16": two of 16.
+cudaError_t k3_n4_h8_s4(const ConvArgs &a, cudaStream_t st);
+cudaError_t k3_n4_h8_c16(const ConvArgs &a, cudaStream_t st);
 cudaError_t k3_tma_f16_w5_h4(const ConvArgs &a, cudaStream_t st);
 cudaError_t k3_tma_f16_w3_h4(const ConvArgs &a, cudaStream_t st);
+cudaError_t k3_tma_f16_w3_h2(const ConvArgs &a, cudaStream_t st);
+cudaError_t k3_tma_f8_w3_h4(const ConvArgs &a, cudaStream_t st);
+cudaError_t k3_tma_f8_w3_h2(const ConvArgs &a, cudaStream_t st);
 cudaError_t k3_tma_f32_w7_h8(const ConvArgs &a, cudaStream_t st);
 cudaError_t k3_tma_f32_w5_h8(const ConvArgs &a, cudaStream_t st);
 cudaError_t k3_tma_f64_w7_h8(const ConvArgs &a, cudaStream_t st);

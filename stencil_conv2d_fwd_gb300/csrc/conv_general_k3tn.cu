@@ -21,6 +21,9 @@ static const TuneCand k3_n16[] = {
     {"F16 W4 8x64", cand_n<16, 4, 8, 64, 1>},
     {"TMA F16 W5 4x80", k3_tma_f16_w5_h4},
     {"TMA F16 W3 4x48", k3_tma_f16_w3_h4},
+    {"TMA F16 W3 2x48", k3_tma_f16_w3_h2},
+    {"TMA F8 W3 4x96", k3_tma_f8_w3_h4},
+    {"TMA F8 W3 2x96", k3_tma_f8_w3_h2},
 };
 static const TuneCand k3_n8[] = {
     {"heuristic", launch_conv_general_k3},
@@ -37,6 +40,10 @@ static const TuneCand k3_n4[] = {
     {"TMA F4 W5 8x160 pc", k3_tma_f4_w5_h8_pc},
     {"TMA F4 W3 4x96 pc", k3_tma_f4_w3_h4_pc},
     {"TMA F4 W5 8x160 r2", k3_tma_f4_w5_h8r2},
+    {"TMA F4 W5 8x160", k3_tma_f4_w5_h8},
+    {"TMA F4 W5 8x160 4 stages", k3_tma_f4_w5_h8_s4},
+    {"N4 W5 8x160 4 stages", k3_n4_h8_s4},
+    {"N4 W5 8x160 c16", k3_n4_h8_c16},
 };
 
 const TuneCand *k3_narrow_table(const ConvArgs &a, int *n)

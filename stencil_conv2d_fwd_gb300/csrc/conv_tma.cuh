@@ -154,24 +154,37 @@ __global__ void __launch_bounds__(C::NT, C::MINB)
     const int nk = cin_pad / C::C_SH;
     const int ntiles = tiles_x * tiles_y * N;
 
-    if (tid == 0) {
-        for (int i = 0; i < C::NSTAGE; ++i) {
-            mbar_init(full(i), 1);
-            mbar_init(empty(i), C::NC);
-        }
-        fence_mbar_init();
-    }
-    tma_issue_filters<C>(w_res, w, co0, cin_pad, Cin, Cout, R, S, tid);
-    cp_async_commit();
-    cp_async_wait<0>();
-    __syncthreads();   // the last block-wide barrier: roles split below
-
     auto decode = [&](int t, int &n, int &y0, int &x0) {
         x0 = (t % tiles_x) * C::TW;
         t /= tiles_x;
         y0 = (t % tiles_y) * C::TH;
         n = t / tiles_y;
     };
+    // copy i of this CTA: step i % nk of tile blockIdx.x + (i / nk) * gridDim.x
+    auto issue = [&](int i, int t, int k) {
+        int n, y0, x0;
+        decode(t, n, y0, x0);
+        const int slot = i % C::NSTAGE;
+        mbar_arrive_expect_tx(full(slot), C::BOX_BYTES);
+        if (i != drop_copy)   // test hook: that copy is never issued
+            tma_load_4d(stage0 + slot * C::STAGE_BYTES, &tm, k * C::C_SH, x0 - C::K / 2, y0 - C::K / 2, n, full(slot));
+    };
+    const int my_tiles = (int)blockIdx.x < ntiles ? (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int pre = my_tiles * nk < C::NSTAGE ? my_tiles * nk : C::NSTAGE;
+    if (warp == C::NC && lane == 0) {
+        for (int i = 0; i < C::NSTAGE; ++i) {
+            mbar_init(full(i), 1);
+            mbar_init(empty(i), C::NC);
+        }
+        fence_mbar_init();
+        // the first copies go out before the filters are staged, so the two
+        // loads overlap
+        for (int i = 0; i < pre; ++i) issue(i, blockIdx.x + (i / nk) * gridDim.x, i % nk);
+    }
+    tma_issue_filters<C>(w_res, w, co0, cin_pad, Cin, Cout, R, S, tid);
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();   // the last block-wide barrier: roles split below
 
     if (warp == C::NC) {
         // ---------------- producer: one thread issues every copy ----------
@@ -179,9 +192,8 @@ __global__ void __launch_bounds__(C::NT, C::MINB)
         int issued = 0;
         bool failed = false;
         for (int t = blockIdx.x; t < ntiles && !failed; t += gridDim.x) {
-            int n, y0, x0;
-            decode(t, n, y0, x0);
             for (int k = 0; k < nk; ++k, ++issued) {
+                if (issued < pre) continue;   // issued before the filters
                 const int slot = issued % C::NSTAGE;
                 if (issued >= C::NSTAGE &&
                     !mbar_wait_bounded(empty(slot), ((issued / C::NSTAGE) - 1) & 1, timeout_ns)) {
@@ -190,10 +202,7 @@ __global__ void __launch_bounds__(C::NT, C::MINB)
                 }
                 // the consumers' reads of this stage come before the copy's writes
                 fence_proxy_async_smem();
-                mbar_arrive_expect_tx(full(slot), C::BOX_BYTES);
-                if (issued != drop_copy)   // test hook: that copy is never issued
-                    tma_load_4d(stage0 + slot * C::STAGE_BYTES, &tm, k * C::C_SH, x0 - C::K / 2, y0 - C::K / 2, n,
-                                full(slot));
+                issue(issued, t, k);
             }
         }
         if (failed) atomicExch(status, kDeviceTimeout);

@@ -44,6 +44,16 @@ cudaError_t k3_tma_f4_w5_h8r2(const ConvArgs &a, cudaStream_t st)
 {
     return launch_conv_tma<TmaCfg<3, 4, 5, 8, 2, 8, 2, 2, false>>(a, st);
 }
+// one CTA a SM with 8 consumer warps: a tile 8 rows high shares its halo
+// rows among more output rows (10 staged rows for 8, against 6 for 4)
+cudaError_t k3_tma_f4_w5_h8(const ConvArgs &a, cudaStream_t st)
+{
+    return launch_conv_tma<TmaCfg<3, 4, 5, 8, 1, 8, 3, 1, false>>(a, st);
+}
+cudaError_t k3_tma_f4_w5_h8_s4(const ConvArgs &a, cudaStream_t st)
+{
+    return launch_conv_tma<TmaCfg<3, 4, 5, 8, 1, 8, 4, 1, false>>(a, st);
+}
 cudaError_t k3_tma_f8_w5_h4(const ConvArgs &a, cudaStream_t st)
 {
     return launch_conv_tma<TmaCfg<3, 8, 5, 4, 1, 8, 3, 2, false>>(a, st);
@@ -55,6 +65,20 @@ cudaError_t k3_tma_f16_w5_h4(const ConvArgs &a, cudaStream_t st)
 cudaError_t k3_tma_f16_w3_h4(const ConvArgs &a, cudaStream_t st)
 {
     return launch_conv_tma<TmaCfg<3, 16, 3, 4, 1, 8, 2, 2, false>>(a, st);
+}
+// small images (16 -> 16 on 128 x 128): more, smaller CTAs so every SM
+// takes part; 8-channel groups or 2-row tiles
+cudaError_t k3_tma_f16_w3_h2(const ConvArgs &a, cudaStream_t st)
+{
+    return launch_conv_tma<TmaCfg<3, 16, 3, 2, 1, 8, 2, 4, false>>(a, st);
+}
+cudaError_t k3_tma_f8_w3_h4(const ConvArgs &a, cudaStream_t st)
+{
+    return launch_conv_tma<TmaCfg<3, 8, 3, 4, 1, 8, 2, 4, false>>(a, st);
+}
+cudaError_t k3_tma_f8_w3_h2(const ConvArgs &a, cudaStream_t st)
+{
+    return launch_conv_tma<TmaCfg<3, 8, 3, 2, 1, 8, 2, 4, false>>(a, st);
 }
 cudaError_t k3_tma_f32_w7_h8(const ConvArgs &a, cudaStream_t st)
 {
@@ -95,7 +119,21 @@ cudaError_t launch_conv_tma_k3_test(const ConvArgs &a, int drop_copy, unsigned l
 // apply (the caller then uses conv_general_k3n.cu's configurations).
 cudaError_t launch_conv_tma_k3_narrow(const ConvArgs &a, cudaStream_t st)
 {
-    if (a.Cout <= 4) return k3_tma_f4_w5_h4(a, st);
+    if (a.Cout <= 4) {
+        // 8 x 160 tiles with one CTA a SM (10 staged rows for 8 output
+        // rows) where they give every SM at least two; 4 output channels
+        // from 32 take the narrow-output kernel (32 -> 4 on 1280 x 720:
+        // 51.9 -> 48.8 us)
+        const long long tiles8 = (long long)((a.W + 159) / 160) * ((a.H + 7) / 8) * a.N;
+        if (tiles8 >= 2LL * device_sm_count()) {
+            if (a.Cout == 4) {
+                const cudaError_t e = k3_n4_h8_s4(a, st);
+                if (e != cudaErrorNotSupported) return e;
+            }
+            return k3_tma_f4_w5_h8_s4(a, st);
+        }
+        return k3_tma_f4_w5_h4(a, st);
+    }
     if (a.Cout <= 8) return k3_tma_f8_w5_h4(a, st);
     // 9-16 channels: 80 x 4 pixel tiles; where those give fewer tiles than
     // the device has SMs, 48 x 4 tiles spread the work over more SMs

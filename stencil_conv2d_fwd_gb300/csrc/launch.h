@@ -67,8 +67,9 @@ cudaError_t launch_stencil_pipeline(const float *in, float *out, int H, int W, c
 cudaError_t launch_transpose_batched(const float *src, float *dst, int N, long long A,
                                      long long B, cudaStream_t st);
 
-// FP32 FMA rate probe (peak.cu).
+// FP32 FMA rate probe and launch-cost probe (peak.cu).
 cudaError_t launch_ffma_peak(float *sink, int blocks, int iters, cudaStream_t st);
+cudaError_t launch_empty(int blocks, int threads, cudaStream_t st);
 
 // Two 3 x 3 layers fused on the tensor cores (conv_tc_fused.cu): x NHWC fp32
 // (C0 channels) -> act1(conv(x, w1) + b1) with C1 = 32 channels, kept on

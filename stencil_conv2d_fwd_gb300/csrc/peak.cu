@@ -23,6 +23,16 @@ __global__ void __launch_bounds__(256) ffma_peak_kernel(float *sink, int iters)
     sink[(size_t)blockIdx.x * blockDim.x + threadIdx.x] = s;
 }
 
+// Launch-cost probe: a kernel that does nothing, so a run of it measures
+// the floor of one launch (back to back, e.g. replayed from a CUDA graph).
+__global__ void empty_kernel() {}
+
+cudaError_t launch_empty(int blocks, int threads, cudaStream_t st)
+{
+    empty_kernel<<<blocks, threads, 0, st>>>();
+    return cudaGetLastError();
+}
+
 cudaError_t launch_ffma_peak(float *sink, int blocks, int iters, cudaStream_t st)
 {
     ffma_peak_kernel<<<blocks, 256, 0, st>>>(sink, iters);

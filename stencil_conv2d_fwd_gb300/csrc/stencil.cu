@@ -304,8 +304,12 @@ __global__ void __launch_bounds__(TS_WARPS * 32)
                 if (yy >= ye) break;
                 const float *rp = sl + j * TS_SW;
                 const float4 own = *reinterpret_cast<const float4 *>(rp + 4 + 4 * lane);
-                float2 lh = *reinterpret_cast<const float2 *>(rp + 2 + 4 * lane);
-                float2 rh = *reinterpret_cast<const float2 *>(rp + 8 + 4 * lane);
+                // halo pixels as in the interior bands: from the neighbour
+                // lanes, the strip's outer two on each side from the slot
+                float2 lh = make_float2(__shfl_up_sync(0xffffffffu, own.z, 1), __shfl_up_sync(0xffffffffu, own.w, 1));
+                float2 rh = make_float2(__shfl_down_sync(0xffffffffu, own.x, 1), __shfl_down_sync(0xffffffffu, own.y, 1));
+                if (lane == 0) lh = *reinterpret_cast<const float2 *>(rp + 2);
+                if (lane == 31) rh = *reinterpret_cast<const float2 *>(rp + 4 + 4 * 32);
                 if (x0 == 0) lh = make_float2(own.x, own.x);          // columns -2, -1
                 if (x0 + 4 >= W) rh = make_float2(own.w, own.w);      // columns W, W+1 (W % 4 == 0)
                 Row8 r;

@@ -117,6 +117,10 @@ SHAPES = [
     (1, 32, 64, 9, 50, 1, 1),
     (2, 8, 4, 5, 7, 1, 1),
     (2, 4, 36, 5, 9, 5, 3),
+    # 32 -> 4 with enough 8 x 160 tiles for the narrow-output kernel: ragged
+    # tiles at the right and bottom edges, several images, a 1 x 3 filter
+    (12, 32, 4, 75, 330, 3, 3),
+    (8, 32, 4, 77, 490, 1, 3),
 ]
 
 

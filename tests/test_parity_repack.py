@@ -11,7 +11,10 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("shape", [(1, 1, 1, 1), (1, 4, 3, 5), (2, 16, 7, 9), (1, 32, 40, 33),
-                                   (3, 64, 5, 70), (1, 5, 31, 33), (1, 100, 3, 3), (2, 4, 128, 128)])
+                                   (3, 64, 5, 70), (1, 5, 31, 33), (1, 100, 3, 3), (2, 4, 128, 128),
+                                   # 16-byte kernel (C % 4 == 0, H * W % 4 == 0): full and ragged
+                                   # 32 x 128 tiles, fewer than 32 channels
+                                   (1, 64, 56, 56), (2, 8, 3, 44), (1, 12, 20, 36), (1, 36, 9, 60)])
 @pytest.mark.parametrize("to_nhwc", [True, False])
 def test_repack(oracle_mod, cuda_dev, sc, shape, to_nhwc):
     N, C, H, W = shape
