@@ -46,6 +46,7 @@ ONLY_CASES = {
     "4-tc": (4, 0), "3-L2-tc": (3, 1), "3-L3-tc": (3, 2),
     "4-bf16": (4, 0), "3-L2-bf16": (3, 1), "3-L3-bf16": (3, 2), "3-L23-fused": (3, 1),
     "4-x3": (4, 0), "3-L2-x3": (3, 1), "3-L3-x3": (3, 2),
+    "S1": (4, "repack"),
 }
 
 
@@ -113,9 +114,9 @@ def kernel_sources(L):
     c = "stencil_conv2d_fwd_gb300/csrc/"
     if L.cin == 1:
         return [c + "conv_c1.cu", c + "common.cuh"]
-    if max(L.r, L.s) == 3:   # the TMA-staged kernel and the dispatch that picks it
+    if max(L.r, L.s) == 3:   # the TMA-staged kernels and the dispatch that picks them
         return [c + "conv_tma.cuh", c + "conv_tma_k3.cu", c + "common.cuh", c + "conv_general_k3.cu",
-                c + "conv_general_k3n.cu"]
+                c + "conv_general_k3n.cu", c + "conv_narrow.cuh", c + "conv_narrow_k3.cu"]
     return [c + "conv_general.cuh", c + "common.cuh", c + f"conv_general_k{max(L.r, L.s)}.cu"]
 
 
@@ -913,7 +914,12 @@ def run_only(args, local):
     sc.load()
     cid, li = ONLY_CASES[args.only]
     wl = S.config(cid)
-    if li is None:
+    if li == "repack":   # S1: the NCHW -> NHWC repack of the workload's input
+        src = torch.from_numpy(np.ascontiguousarray(wl.x)).to(dev)
+        dst = torch.empty_like(src)
+        n_, c_, h_, w_ = wl.x.shape
+        launch = lambda: sc.sc_repack(src, dst, n_, c_, h_, w_, sc.SC_NCHW, sc.SC_NHWC)
+    elif li is None:
         ind = torch.from_numpy(wl.img).to(dev)
         outd = torch.empty_like(ind)
         launch = lambda: sc.stencil_pipeline_fwd(ind, outd, wl.h, wl.w)
