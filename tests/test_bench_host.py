@@ -77,7 +77,8 @@ def test_per_config_summary_keys_are_unique_and_short():
     pc = {"launch_floor": {"us_per_launch": 0.56},
           "1: 64x64 1->1 3x3": {"ms_mean": 0.0061, "roofline_frac": 0.001, "graph_ms_per_launch": 0.0015,
                                 "launch_floor_us": 0.56},
-          "3-L3: 1280x720 32->4 3x3": {"ms_mean": 0.05, "roofline_frac": 0.52},
+          "3-L3: 1280x720 32->4 3x3": {"ms_mean": 0.05, "roofline_frac": 0.52, "ms_kernel": 0.045,
+                                       "roofline_frac_kernel": 0.58},
           "3: 3-layer net replayed as a CUDA graph": {"ms_mean": 0.36},
           "3: 3-layer net, layers 2 and 3 on split-TF32 tensor cores": {"ms_mean": 0.16},
           "4 (tcgen05 TF32)": {"ms_mean": 0.024, "roofline_frac": 0.32},
@@ -85,6 +86,6 @@ def test_per_config_summary_keys_are_unique_and_short():
           "3-L2 (tcgen05 BF16, bf16 x/y)": {"ms_mean": 0.035, "roofline_frac": 0.5},
           "_peaks": {"fp32_tflops": 80.5}}
     s = bench.per_config_summary(pc)
-    assert s == {"1": [0.0061, 0.001, 0.0015, 0.56], "3-L3": [0.05, 0.52], "3 graph": [0.36, None],
+    assert s == {"1": [0.0061, 0.001, 0.0015, 0.56], "3-L3": [0.05, 0.52, 0.045, 0.58], "3 graph": [0.36, None],
                  "3 x3 net": [0.16, None], "4 tf32": [0.024, 0.32], "4 x3": [0.064, 0.37],
                  "3-L2 bf16": [0.035, 0.5]}
