@@ -82,16 +82,19 @@ def test_bf16_shapes(oracle_mod, cuda_dev, sc, shape, y_dtype):
     assert_conv_close(y, yr, tol_scale(yr, a, y_dtype), rtol=BF16_RTOL, what=f"bf16 {shape} y_dtype={y_dtype}")
 
 
+@pytest.mark.parametrize("y_dtype", [1, 0], ids=["y_bf16", "y_f32"])
 @pytest.mark.parametrize("cid,li", [(4, 0), (3, 1), (3, 2)])
-def test_bf16_workloads_full_size(oracle_mod, cuda_dev, sc, cid, li):
+def test_bf16_workloads_full_size(oracle_mod, cuda_dev, sc, cid, li, y_dtype):
+    """Full workload sizes.  With y_f32 the bound is the plain 5e-3 * A of the
+    tensor-core variants (no storage term): the computation alone."""
     wl = S.config(cid)
     L = wl.layers[li]
     x = wl.x if li == 0 else np.maximum(S.uniform(77, 0, (wl.n, L.cin, wl.h, wl.w), -1, 1), 0).astype(np.float32)
     x = round_to_bf16(x)
-    y = conv_bf16(x, L.w, L.b, L.act, sc.SC_BF16, cuda_dev)
+    y = conv_bf16(x, L.w, L.b, L.act, y_dtype, cuda_dev)
     yr, a = oracle_mod.conv2d_nchw(x, L.w, L.b, L.act)
-    worst = assert_conv_close(y, yr, tol_scale(yr, a, sc.SC_BF16), rtol=BF16_RTOL,
-                              what=f"bf16 workload {cid} layer {li}")
+    worst = assert_conv_close(y, yr, tol_scale(yr, a, y_dtype), rtol=BF16_RTOL,
+                              what=f"bf16 workload {cid} layer {li} y_dtype={y_dtype}")
     assert worst < 1.0
 
 
