@@ -116,7 +116,7 @@ def kernel_sources(L):
         return [c + "conv_c1.cu", c + "common.cuh"]
     if max(L.r, L.s) == 3:   # the TMA-staged kernels and the dispatch that picks them
         return [c + "conv_tma.cuh", c + "conv_tma_k3.cu", c + "common.cuh", c + "conv_general_k3.cu",
-                c + "conv_general_k3n.cu", c + "conv_narrow.cuh", c + "conv_narrow_k3.cu"]
+                c + "conv_general_k3n.cu", c + "conv_narrow.cuh", c + "conv_narrow_k3.cu", c + "conv_small.cu"]
     return [c + "conv_general.cuh", c + "common.cuh", c + f"conv_general_k{max(L.r, L.s)}.cu"]
 
 

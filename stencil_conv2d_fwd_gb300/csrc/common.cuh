@@ -55,6 +55,14 @@ SC_HD int tma_swz_key(int p, int c_sh) { return (p * c_sh / 32) & (c_sh / 4 - 1)
 // of an even number of chunks.
 SC_HD int c1_band_chunk(int L) { return L ^ ((L >> 3) & 1); }
 
+// conv_small.cu stages a tile row of 66 pixels x 4 16-byte chunks (16
+// channels); lanes 8 c + q read pixel 8 q + k, so the eight pixel runs of
+// a quarter-warp ask for chunks 32 apart, all in one bank group (chunk mod
+// 8).  Chunk 4 p + cb is stored at (4 p + cb) XOR ((p / 8) mod 8): the XOR
+// only touches the low 3 bits, so it permutes each aligned group of 8
+// chunks (one pixel pair), and over q it adds q mod 8 to the bank group.
+SC_HD int small_tile_chunk(int p, int cb) { return (4 * p + cb) ^ ((p >> 3) & 7); }
+
 #if defined(__CUDACC__)
 
 // ---------------------------------------------------------------------------

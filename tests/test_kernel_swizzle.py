@@ -26,7 +26,8 @@ def swz(tmp_path_factory):
                    'extern "C" int h_swz16(int i, int L) { return sc::swz16(i, L); }\n'
                    'extern "C" int h_swz_col(int r, int c, int L) { return sc::swz_col(r, c, L); }\n'
                    'extern "C" int h_tma_key(int p, int c) { return sc::tma_swz_key(p, c); }\n'
-                   'extern "C" int h_c1_band_chunk(int L) { return sc::c1_band_chunk(L); }\n')
+                   'extern "C" int h_c1_band_chunk(int L) { return sc::c1_band_chunk(L); }\n'
+                   'extern "C" int h_small_tile_chunk(int p, int cb) { return sc::small_tile_chunk(p, cb); }\n')
     so = d / "libswz.so"
     subprocess.run(["g++", "-std=c++17", "-O1", "-fPIC", "-shared", str(src), "-o", str(so)], check=True)
     lib = ctypes.CDLL(str(so))
@@ -34,6 +35,7 @@ def swz(tmp_path_factory):
     lib.h_swz_col.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
     lib.h_tma_key.argtypes = [ctypes.c_int, ctypes.c_int]
     lib.h_c1_band_chunk.argtypes = [ctypes.c_int]
+    lib.h_small_tile_chunk.argtypes = [ctypes.c_int, ctypes.c_int]
     return lib
 
 
@@ -353,3 +355,45 @@ def test_c1_tile_output_buffer_is_the_store_copy_box():
             for q in range(8):
                 want = tma_swizzled_byte(row * 128 + 16 * q, 128)
                 assert want == row * 128 + 16 * (q ^ g)
+
+
+# ---------------------------------------------------------------------------
+# conv_small.cu, conv_small_kernel: lane = 8 c + q (output-channel quad c, one
+# per quarter-warp; pixel run q of 8 pixels), a staged tile row of 66 pixels x
+# 4 chunks of 4 channels, filters [ci][tap][16 outputs], exchanged partial
+# sums as float4 [row][owner][slot][pair][lane].
+
+def test_small_tile_chunk_is_one_to_one_on_a_row(swz):
+    got = sorted(swz.h_small_tile_chunk(p, cb) for p in range(66) for cb in range(4))
+    assert got == list(range(264))
+
+
+@pytest.mark.parametrize("k", range(10))
+@pytest.mark.parametrize("grp", range(4))
+def test_small_tile_pixel_reads_conflict_free(swz, k, grp):
+    """Staged pixel 8 q + k, chunk grp: eight distinct chunks per quarter-warp
+    (the four quarter-warps ask for the same eight), in eight bank groups."""
+    chunks = [swz.h_small_tile_chunk(8 * (l & 7) + k, grp) for l in range(32)]
+    assert conflict_free_128bit(chunks)
+    assert wavefronts_128bit(chunks) == 4
+
+
+def test_small_tile_unswizzled_pixel_reads_would_conflict():
+    chunks = [4 * (8 * (l & 7)) for l in range(32)]
+    assert wavefronts_128bit(chunks) == 32
+
+
+def test_small_filter_and_partial_sum_accesses():
+    """Filter chunk (ci 9 + tap) 4 + c: one chunk per quarter-warp, two
+    wavefronts; partial-sum chunk (slot index) 32 + lane: 32 contiguous
+    chunks; filter staging stores word (ci 9 + tap) 16 + co with co = tid %
+    16, ci = tid / 16: a warp's 32 stores in 32 distinct banks."""
+    for base in (0, 4 * 9 * 3 + 4 * 5):
+        assert wavefronts_128bit([base + (l >> 3) for l in range(32)]) == 2
+    for f in range(4):
+        chunks = [f * 32 + l for l in range(32)]
+        assert phases_conflict_free(chunks) and wavefronts_128bit(chunks) == 4
+    for warp in range(8):
+        for tap in range(9):
+            words = [((t // 16) * 9 + tap) * 16 + t % 16 for t in range(32 * warp, 32 * warp + 32)]
+            assert len({wd % 32 for wd in words}) == 32

@@ -121,6 +121,15 @@ SHAPES = [
     # tiles at the right and bottom edges, several images, a 1 x 3 filter
     (12, 32, 4, 75, 330, 3, 3),
     (8, 32, 4, 77, 490, 1, 3),
+    # small images, at most 16 channels in and out (whole-tile kernel):
+    # ragged 4 x 32 tiles, several images, fewer channels than 16, 1 x 3 and
+    # 3 x 1 filters, and the largest image it takes (64 K pixels)
+    (4, 12, 8, 30, 50, 3, 3),
+    (1, 16, 12, 7, 97, 1, 3),
+    (1, 4, 16, 5, 33, 3, 1),
+    (2, 16, 4, 100, 40, 3, 3),
+    (1, 16, 16, 256, 256, 3, 3),
+    (1, 16, 16, 257, 256, 3, 3),
 ]
 
 
