@@ -173,6 +173,22 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// As mbar_wait_bounded, for a thread with nothing else to do (a producer
+// waiting for a stage to be released): between polls it sleeps about
+// sleep_ns, so that its polling takes few issue slots from the warps that
+// share its scheduler.
+__device__ __forceinline__ bool mbar_wait_bounded_idle(uint32_t bar, uint32_t parity,
+                                                       unsigned long long timeout_ns, unsigned sleep_ns)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+        __nanosleep(sleep_ns);
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > timeout_ns) return false;
+    }
+}
+
 // Order this thread's earlier generic-proxy shared-memory accesses before
 // later async-proxy (TMA) accesses to the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem()

@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(C::NT, C::MINB)
         int i = pre;
         for (; i < total; ++i) {
             const int slot = i % C::NSTAGE;
-            if (!mbar_wait_bounded(empty(slot), ((i / C::NSTAGE) - 1) & 1, timeout_ns)) {
+            if (!mbar_wait_bounded_idle(empty(slot), ((i / C::NSTAGE) - 1) & 1, timeout_ns, 64)) {
                 failed = true;
                 break;
             }

@@ -1,5 +1,5 @@
 // Direct convolution for small images (up to 64 K pixels in all) with up to
-// 16 input and 16 output channels and filters up to 3 x 3: the shape of a
+// 16 input and 16 output channels and 3 x 3 filters: the shape of a
 // single small CNN layer, whose whole work (16 -> 16 on 128 x 128: 75
 // MFLOP) is about a microsecond of the GPU's FP32 rate, so that a launch is
 // dominated by its fixed costs (starting the CTAs, one round trip to memory,
@@ -14,9 +14,10 @@
 //    split the tile's rows (2) and the input channels (4 groups of 4), so a
 //    thread computes 8 pixels x 4 output channels over 4 input channels;
 //  * every copy is issued at once and waited for once: the input tile by
-//    16-byte asynchronous copies, the filter bank by each thread loading the
-//    9 taps of one (output, input) channel pair and storing them transposed
-//    to [ci][tap][co];
+//    16-byte asynchronous copies, the filter bank by loads along its OIHW
+//    order (a warp-wide load is one 128-byte line; loads with a lane per
+//    output channel touched 32 lines each and took 1.4 us of L1 lookups per
+//    CTA) stored transposed to [ci][tap][co] at a row pitch of 20 floats;
 //  * the four input-channel groups' partial sums are exchanged through
 //    shared memory so that each warp finishes and stores 2 of its row's 8
 //    pixels per thread: two barriers in all.
@@ -45,23 +46,22 @@ constexpr int SM_PW = SM_TW + 2;                                  // staged pixe
 constexpr int SM_MAXC = 16;                                       // input and output channels at most
 constexpr long long SM_MAX_PIXELS = 1LL << 16;                    // N * H * W up to which it is used
 constexpr int SM_XS_FLOATS = (SM_TH + 2) * SM_PW * SM_MAXC;       // staged input rows
-constexpr int SM_WS_FLOATS = SM_MAXC * 9 * SM_MAXC;               // filters [ci][tap][co]
+constexpr int SM_WP = 20;                                         // filter row pitch: 16 outputs + 4
+constexpr int SM_WS_FLOATS = SM_MAXC * 9 * SM_WP;                 // filters [ci][tap][co]
 constexpr int SM_PART_F4 = SM_TH * SM_CIG * (SM_CIG - 1) * 2 * 32; // exchanged partial sums
 constexpr int SM_SMEM = (SM_XS_FLOATS + SM_WS_FLOATS) * 4 + SM_PART_F4 * 16;
-static_assert(SM_NT == SM_MAXC * SM_MAXC, "one (output, input) channel pair of filters per thread");
 static_assert(SM_PW * 4 % 8 == 0, "a staged row is whole groups of 8 chunks (small_tile_chunk)");
 }  // namespace
 
 template <int CB>   // input channels / 4
 __global__ void __launch_bounds__(SM_NT, 1)
     conv_small_kernel(const float *__restrict__ x, const float *__restrict__ w, const float *__restrict__ bias,
-                      float *__restrict__ y, int H, int W, int Cout, int R, int S, int act, int tiles_x,
-                      int tiles_y)
+                      float *__restrict__ y, int H, int W, int Cout, int act, int tiles_x, int tiles_y)
 {
     constexpr int Cin = 4 * CB;
     extern __shared__ __align__(16) float small_smem[];
     float *xs = small_smem;                                              // [row][small_tile_chunk(p, cb)]
-    float *ws = xs + SM_XS_FLOATS;                                       // [ci][tap][16 outputs]
+    float *ws = xs + SM_XS_FLOATS;                                       // [ci * 9 + tap][co], pitch SM_WP
     float4 *part = reinterpret_cast<float4 *>(ws + SM_WS_FLOATS);       // [row][owner][slot][pair][lane]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int t = blockIdx.x;
@@ -84,20 +84,20 @@ __global__ void __launch_bounds__(SM_NT, 1)
     float4 bv = make_float4(0.f, 0.f, 0.f, 0.f);
     if (bias && 4 * c < Cout) bv = make_float4(bias[4 * c], bias[4 * c + 1], bias[4 * c + 2], bias[4 * c + 3]);
     {
-        // filters of channel pair (co, ci), the R x S filter centred in 3 x 3
-        // and zeros elsewhere; a warp's stores are 32 distinct banks
-        const int co = tid % SM_MAXC, ci = tid / SM_MAXC;
-        if (co < Cout && ci < Cin) {
-            const int dr = (3 - R) / 2, ds = (3 - S) / 2;
-            const float *src = w + ((long long)co * Cin + ci) * R * S;
-            float wv[9];
+        // the filter bank in its OIHW order, element e = co * 9 Cin + k with
+        // k = ci * 9 + tap, to word k * SM_WP + co: a warp's 32 stores fall
+        // in 8 banks (the 20-float pitch; 16 would put them in one)
+        constexpr int KK = Cin * 9, NV = (SM_MAXC * KK + SM_NT - 1) / SM_NT;
+        float wv[NV];
 #pragma unroll
-            for (int tap = 0; tap < 9; ++tap) {
-                const int r = tap / 3 - dr, s = tap % 3 - ds;
-                wv[tap] = (r >= 0 && r < R && s >= 0 && s < S) ? __ldg(src + r * S + s) : 0.f;
-            }
+        for (int m = 0; m < NV; ++m) {
+            const int e = tid + m * SM_NT;
+            wv[m] = e < Cout * KK ? __ldg(w + e) : 0.f;
+        }
 #pragma unroll
-            for (int tap = 0; tap < 9; ++tap) ws[(ci * 9 + tap) * SM_MAXC + co] = wv[tap];
+        for (int m = 0; m < NV; ++m) {
+            const int e = tid + m * SM_NT;
+            if (e < Cout * KK) ws[(e % KK) * SM_WP + e / KK] = wv[m];
         }
     }
     cp_async_wait<0>();
@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(SM_NT, 1)
         for (int j = 0; j < SM_PT; ++j) acc[f][j] = 0.f;
     if (grp < CB && 4 * c < Cout) {
         const float *xrow = xs + row * SM_PW * SM_MAXC;
-        const float *wg = ws + (4 * grp * 9) * SM_MAXC + 4 * c;
+        const float *wg = ws + (4 * grp * 9) * SM_WP + 4 * c;
 #pragma unroll
         for (int r = 0; r < 3; ++r) {
             // staged pixels 8 q .. 8 q + 9 (image columns x - 1 .. x + 8), channels 4 grp .. 4 grp + 3
@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(SM_NT, 1)
             for (int ci = 0; ci < 4; ++ci)
 #pragma unroll
                 for (int s = 0; s < 3; ++s) {
-                    const float4 wv = *reinterpret_cast<const float4 *>(wg + (ci * 9 + 3 * r + s) * SM_MAXC);
+                    const float4 wv = *reinterpret_cast<const float4 *>(wg + (ci * 9 + 3 * r + s) * SM_WP);
 #pragma unroll
                     for (int j = 0; j < SM_PT; ++j) {
                         const float4 p = px[j + s];
@@ -198,16 +198,16 @@ static cudaError_t launch_small(const ConvArgs &a, int tiles_x, int tiles_y, uns
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     e = ensure_dynamic_smem(cache, dev, conv_small_kernel<CB>, SM_SMEM);
     if (e != cudaSuccess) return e;
-    conv_small_kernel<CB><<<nb, SM_NT, SM_SMEM, st>>>(a.x, a.w, a.b, a.y, a.H, a.W, a.Cout, a.R, a.S, a.act,
-                                                      tiles_x, tiles_y);
+    conv_small_kernel<CB><<<nb, SM_NT, SM_SMEM, st>>>(a.x, a.w, a.b, a.y, a.H, a.W, a.Cout, a.act, tiles_x,
+                                                      tiles_y);
     return cudaGetLastError();
 }
 
-// NHWC, Cin and Cout multiples of 4 up to 16, filters up to 3 x 3, at most
-// 64 K pixels in all; cudaErrorNotSupported otherwise.
+// NHWC, Cin and Cout multiples of 4 up to 16, 3 x 3 filters, at most 64 K
+// pixels in all; cudaErrorNotSupported otherwise.
 cudaError_t launch_conv_small(const ConvArgs &a, cudaStream_t st)
 {
-    if (a.Cin % 4 || a.Cout % 4 || a.Cin > SM_MAXC || a.Cout > SM_MAXC || a.R > 3 || a.S > 3 ||
+    if (a.Cin % 4 || a.Cout % 4 || a.Cin > SM_MAXC || a.Cout > SM_MAXC || a.R != 3 || a.S != 3 ||
         (long long)a.N * a.H * a.W > SM_MAX_PIXELS)
         return cudaErrorNotSupported;
     const int tiles_x = (a.W + SM_TW - 1) / SM_TW, tiles_y = (a.H + SM_TH - 1) / SM_TH;

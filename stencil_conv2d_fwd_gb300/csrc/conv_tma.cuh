@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(C::NT, C::MINB)
                 if (issued < pre) continue;   // issued before the filters
                 const int slot = issued % C::NSTAGE;
                 if (issued >= C::NSTAGE &&
-                    !mbar_wait_bounded(empty(slot), ((issued / C::NSTAGE) - 1) & 1, timeout_ns)) {
+                    !mbar_wait_bounded_idle(empty(slot), ((issued / C::NSTAGE) - 1) & 1, timeout_ns, 64)) {
                     failed = true;
                     break;
                 }

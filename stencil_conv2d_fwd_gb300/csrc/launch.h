@@ -29,8 +29,8 @@ cudaError_t launch_conv_general_k7(const ConvArgs &a, cudaStream_t st);
 // where it does not apply.
 cudaError_t launch_conv_tma_k3_narrow(const ConvArgs &a, cudaStream_t st);
 // Whole-tile-at-once direct convolution for small images (conv_small.cu):
-// NHWC, Cin and Cout multiples of 4 up to 16, filters up to 3 x 3, at most
-// 64 K pixels in all; cudaErrorNotSupported otherwise.
+// NHWC, Cin and Cout multiples of 4 up to 16, 3 x 3 filters, at most 64 K
+// pixels in all; cudaErrorNotSupported otherwise.
 cudaError_t launch_conv_small(const ConvArgs &a, cudaStream_t st);
 cudaError_t launch_conv_tma_k3_wide(const ConvArgs &a, cudaStream_t st);
 // The same kernel for 5 x 5 filters with 16 or fewer output channels and for

@@ -384,16 +384,22 @@ def test_small_tile_unswizzled_pixel_reads_would_conflict():
 
 
 def test_small_filter_and_partial_sum_accesses():
-    """Filter chunk (ci 9 + tap) 4 + c: one chunk per quarter-warp, two
-    wavefronts; partial-sum chunk (slot index) 32 + lane: 32 contiguous
-    chunks; filter staging stores word (ci 9 + tap) 16 + co with co = tid %
-    16, ci = tid / 16: a warp's 32 stores in 32 distinct banks."""
-    for base in (0, 4 * 9 * 3 + 4 * 5):
-        assert wavefronts_128bit([base + (l >> 3) for l in range(32)]) == 2
+    """Filter chunk ((ci 9 + tap) 20 + 4 c) / 4: one chunk per quarter-warp,
+    two wavefronts; partial-sum chunk (slot index) 32 + lane: 32 contiguous
+    chunks; filter staging stores element e = co 9 Cin + k of the OIHW bank
+    to word k 20 + co, lanes along e: at most 4 lanes of a warp per bank."""
+    for ci in range(16):
+        for tap in range(9):
+            chunks = [((ci * 9 + tap) * 20 + 4 * (l >> 3)) // 4 for l in range(32)]
+            assert wavefronts_128bit(chunks) == 2 and conflict_free_128bit(chunks)
     for f in range(4):
         chunks = [f * 32 + l for l in range(32)]
         assert phases_conflict_free(chunks) and wavefronts_128bit(chunks) == 4
-    for warp in range(8):
-        for tap in range(9):
-            words = [((t // 16) * 9 + tap) * 16 + t % 16 for t in range(32 * warp, 32 * warp + 32)]
-            assert len({wd % 32 for wd in words}) == 32
+    for cin in (4, 8, 12, 16):
+        KK = 9 * cin
+        for warp in range(0, 16 * KK // 32 + 1):
+            es = [e for e in range(32 * warp, 32 * warp + 32) if e < 16 * KK]
+            if not es:
+                continue
+            banks = [((e % KK) * 20 + e // KK) % 32 for e in es]
+            assert max(banks.count(bk) for bk in set(banks)) <= 4
