@@ -408,13 +408,17 @@ __global__ void __launch_bounds__(C::NT, C::MINB)
             if (lane == 0) mbar_arrive(empty(slot));
         }
 
-        // epilogue: bias, activation, 16-byte NHWC stores of 4 output channels
+        // epilogue: bias, activation, 16-byte NHWC stores of 4 output
+        // channels; a group's W_T values are formed before its first store,
+        // and rows inside the image store without per-pixel tests (32 -> 32
+        // on 1280 x 720: 279.6 -> 275.1 us)
         auto res = [&](int h, int f, int j) {
             if constexpr (C::PAIRC) return acc2[h][f][j].x + acc2[h][f][j].y;
             else return acc[h][f][j];
         };
         int n, y0, x0;
         decode(t, n, y0, x0);
+        const bool full_row = x0 + cx0 + C::W_T <= W;
 #pragma unroll
         for (int h = 0; h < C::H_T; ++h) {
             const int gy = y0 + warp * C::H_T + h;
@@ -423,17 +427,22 @@ __global__ void __launch_bounds__(C::NT, C::MINB)
                 for (int g = 0; g < C::NG; ++g) {
                     const int co = co0 + g * (C::F_TB / C::NG) + 4 * tx;
                     if (co < Cout) {
+                        float4 o[C::W_T];
 #pragma unroll
                         for (int j = 0; j < C::W_T; ++j) {
-                            const int gx = x0 + cx0 + j;
-                            if (gx < W) {
-                                float4 o;
-                                o.x = relu_if(res(h, 4 * g + 0, j) + bv[4 * g + 0], act);
-                                o.y = relu_if(res(h, 4 * g + 1, j) + bv[4 * g + 1], act);
-                                o.z = relu_if(res(h, 4 * g + 2, j) + bv[4 * g + 2], act);
-                                o.w = relu_if(res(h, 4 * g + 3, j) + bv[4 * g + 3], act);
-                                *reinterpret_cast<float4 *>(y + ((((long long)n * H + gy) * W + gx) * Cout + co)) = o;
-                            }
+                            o[j].x = relu_if(res(h, 4 * g + 0, j) + bv[4 * g + 0], act);
+                            o[j].y = relu_if(res(h, 4 * g + 1, j) + bv[4 * g + 1], act);
+                            o[j].z = relu_if(res(h, 4 * g + 2, j) + bv[4 * g + 2], act);
+                            o[j].w = relu_if(res(h, 4 * g + 3, j) + bv[4 * g + 3], act);
+                        }
+                        float *yp = y + ((((long long)n * H + gy) * W + x0 + cx0) * Cout + co);
+                        if (full_row) {
+#pragma unroll
+                            for (int j = 0; j < C::W_T; ++j) *reinterpret_cast<float4 *>(yp + (long long)j * Cout) = o[j];
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < C::W_T; ++j)
+                                if (x0 + cx0 + j < W) *reinterpret_cast<float4 *>(yp + (long long)j * Cout) = o[j];
                         }
                     }
                 }
