@@ -106,6 +106,37 @@ def test_tma_candidates_at_their_edges(oracle_mod, cuda_dev, sc, shape):
     assert sc.sc_last_device_status() == sc.SC_OK
 
 
+N4_MANY_TILES = [
+    # (N, Cin, Cout, H, W): 32 -> 4 with more 8 x 160 tiles than CTAs, so the
+    # narrow-output kernels' CTAs take several tiles (tile pairs and an odd
+    # last tile in the two-rows-per-warp kernel); ragged right and bottom
+    # edges, several images
+    (12, 32, 4, 75, 330),
+    (5, 32, 4, 41, 1281),
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("shape", N4_MANY_TILES, ids=[str(s) for s in N4_MANY_TILES])
+@pytest.mark.parametrize("act", [0, 1])
+def test_narrow_output_candidates_with_many_tiles(oracle_mod, cuda_dev, sc, shape, act):
+    N, Cin, Cout, H, W = shape
+    c = S.conv_case(980 + W + act, N, Cin, Cout, H, W, 3, 3, act=act)
+    L = c.layers[0]
+    yr, a = oracle_mod.conv2d_nchw(c.x, L.w, L.b, L.act)
+    names = sc.sc_autotune_candidates(Cin, Cout, 3, 3)
+    ran = 0
+    for i, name in enumerate(names):
+        if not name.startswith("N4"):
+            continue
+        rc, y = _run_candidate(c.x, L.w, L.b, L.act, i, cuda_dev)
+        assert rc == sc.SC_OK, (name, sc.sc_status_string(rc))
+        assert_conv_close(y, yr, a, what=f"candidate {i} ({name}) {shape}")
+        ran += 1
+    assert ran >= 3
+    assert sc.sc_last_device_status() == sc.SC_OK
+
+
 @pytest.mark.gpu
 def test_tuned_call_caches_its_choice_and_repeats(oracle_mod, cuda_dev, sc):
     N, Cin, Cout, H, W = 1, 32, 32, 23, 97
