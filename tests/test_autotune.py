@@ -108,9 +108,9 @@ def test_tma_candidates_at_their_edges(oracle_mod, cuda_dev, sc, shape):
 
 N4_MANY_TILES = [
     # (N, Cin, Cout, H, W): 32 -> 4 with more 8 x 160 tiles than CTAs, so the
-    # narrow-output kernels' CTAs take several tiles (tile pairs and an odd
-    # last tile in the two-rows-per-warp kernel); ragged right and bottom
-    # edges, several images
+    # narrow-output kernels' CTAs take several tiles (the cross-step prefetch
+    # runs across tile boundaries); ragged right and bottom edges, several
+    # images
     (12, 32, 4, 75, 330),
     (5, 32, 4, 41, 1281),
 ]
@@ -133,7 +133,7 @@ def test_narrow_output_candidates_with_many_tiles(oracle_mod, cuda_dev, sc, shap
         assert rc == sc.SC_OK, (name, sc.sc_status_string(rc))
         assert_conv_close(y, yr, a, what=f"candidate {i} ({name}) {shape}")
         ran += 1
-    assert ran >= 3
+    assert ran >= 2
     assert sc.sc_last_device_status() == sc.SC_OK
 
 
