@@ -78,6 +78,50 @@ int conv2d_fwd(const float *x, const float *w, const float *b, float *y,
                int layout, int act, sc_stream_t stream);
 
 /*
+ * One layer of a convolution chain (conv2d_chain_fwd_host): filters w
+ * (device memory, [Cout][Cin][R][S] fp32 with Cin the previous layer's
+ * output channels), bias b (device memory, Cout floats, or NULL), the
+ * filter size R x S and the activation (SC_ACT_NONE or SC_ACT_RELU).
+ */
+typedef struct {
+    const float *w;
+    const float *b;
+    int Cout, R, S, act;
+} sc_conv_layer;
+
+#define SC_CHAIN_MAX_LAYERS 64
+
+/*
+ * conv2d_chain_fwd_host: a chain of convolution layers run on an input in
+ * host memory, the result returned to host memory, as a network like the
+ * upscaling network of "Optimizing convolution kernels - CNNs in Vulkan
+ * Part 2/3" (opening paragraphs and "Where we left off": one image through
+ * its layers in turn, each layer's output the next one's input):
+ *   a_0 = x,  a_l = act_l(conv(a_{l-1}, w_l) + b_l) for l = 1..n_layers,
+ *   y = a_{n_layers},
+ * each conv exactly conv2d_fwd's (stride 1, zero "same" padding, NHWC).
+ * On `stream`, in order: x_host is copied to the device, the layers run
+ * with their activations in stream-ordered device buffers from the
+ * library's memory pool (freed on `stream` after use; see
+ * sc_release_workspace), and the last layer's output is copied to y_host.
+ * The call returns once this is enqueued: x_host must stay unchanged and
+ * y_host unread until the stream has completed it.  With page-locked
+ * (pinned) host buffers both copies are asynchronous DMA transfers; with
+ * pageable ones the CUDA runtime stages them and the call may wait for
+ * the copies.
+ * x_host : N*H*W*Cin floats, NHWC.  y_host : N*H*W*Cout floats of the last
+ *   layer, NHWC.  layers : n_layers entries, 1 <= n_layers <=
+ *   SC_CHAIN_MAX_LAYERS.
+ * Every layer's shape is checked (conv2d_fwd's rules, with its Cin the
+ * previous layer's Cout) before anything is enqueued: SC_ERR_NULL for a
+ * NULL x_host, y_host, layers or w, SC_ERR_SHAPE / SC_ERR_UNSUPPORTED as
+ * conv2d_fwd, SC_ERR_SHAPE for n_layers out of range.  A failed CUDA call
+ * returns SC_ERR_CUDA (code in sc_last_cuda_error).
+ */
+int conv2d_chain_fwd_host(const float *x_host, float *y_host, int N, int H, int W, int Cin,
+                          int n_layers, const sc_conv_layer *layers, sc_stream_t stream);
+
+/*
  * conv2d_fwd_tc: the same operation as conv2d_fwd on the tensor cores
  * (tcgen05 MMA, accumulators in tensor memory) as an implicit GEMM
  * (pixels x output channels x (taps, input channels); "Optimizing Memory

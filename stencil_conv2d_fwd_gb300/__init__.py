@@ -60,7 +60,15 @@ SIGNATURES = {
     "sc_test_stencil_wait_expiry": (_I, [_P, _P, _I, _I, _I, _I, _P]),
     "sc_test_conv_wait_expiry": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
     "sc_test_workspace_allocs": (ctypes.c_longlong, []),
+    "conv2d_chain_fwd_host": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P]),
 }
+SC_CHAIN_MAX_LAYERS = 64
+
+
+class ScConvLayer(ctypes.Structure):
+    """sc_conv_layer: one layer of conv2d_chain_fwd_host (device filters and bias)."""
+    _fields_ = [("w", ctypes.c_void_p), ("b", ctypes.c_void_p), ("Cout", ctypes.c_int), ("R", ctypes.c_int),
+                ("S", ctypes.c_int), ("act", ctypes.c_int)]
 SC_NOALLOC_SCRATCH_FLOATS = 8 * 1024 * 1024
 
 _lib = None
@@ -210,6 +218,19 @@ def conv2d_fwd_nchw_noalloc(x, w, b, y, N, H, W, Cin, Cout, R, S, act=SC_ACT_NON
     """NCHW conv2d_fwd that allocates no device memory (see the header)."""
     return load().conv2d_fwd_nchw_noalloc(_ptr(x), _ptr(w), _ptr(b), _ptr(y), N, H, W, Cin, Cout, R, S,
                                           act, _stream(stream))
+
+
+def conv2d_chain_fwd_host(x_host, y_host, N, H, W, Cin, layers, stream=None) -> int:
+    """Layers run in turn on a host-resident NHWC input, result to host memory.
+
+    x_host / y_host: host tensors (pinned for asynchronous copies) or raw host
+    addresses; layers: sequence of (w, b, Cout, R, S, act) with w and b device
+    tensors or addresses (b may be None).  See the header."""
+    arr = (ScConvLayer * max(len(layers), 1))()
+    for i, (w, b, cout, r, s_, act) in enumerate(layers):
+        arr[i] = ScConvLayer(_ptr(w), _ptr(b), cout, r, s_, act)
+    return load().conv2d_chain_fwd_host(_ptr(x_host), _ptr(y_host), N, H, W, Cin, len(layers),
+                                        ctypes.cast(arr, ctypes.c_void_p), _stream(stream))
 
 
 def sc_empty_kernel(blocks, threads, stream=None) -> int:

@@ -63,10 +63,8 @@ int record_cuda_error(cudaError_t e)
     return SC_ERR_CUDA;
 }
 
-int check_conv_args(const float *x, const float *w, const float *b, const float *y, int N, int H, int W, int Cin,
-                    int Cout, int R, int S, int layout, int act)
+int check_conv_shape(int N, int H, int W, int Cin, int Cout, int R, int S, int layout, int act)
 {
-    if (!x || !w || !y) return SC_ERR_NULL;
     const long long nx = checked_count({N, H, W, Cin});
     const long long ny = checked_count({N, H, W, Cout});
     const long long nw = checked_count({Cout, Cin, R, S});
@@ -80,6 +78,17 @@ int check_conv_args(const float *x, const float *w, const float *b, const float 
     } else {
         if ((Cin % 4) != 0 || (Cout % 4) != 0) return SC_ERR_UNSUPPORTED;
     }
+    return SC_OK;
+}
+
+int check_conv_args(const float *x, const float *w, const float *b, const float *y, int N, int H, int W, int Cin,
+                    int Cout, int R, int S, int layout, int act)
+{
+    if (!x || !w || !y) return SC_ERR_NULL;
+    const int shape = check_conv_shape(N, H, W, Cin, Cout, R, S, layout, act);
+    if (shape != SC_OK) return shape;
+    const long long nx = (long long)N * H * W * Cin, ny = (long long)N * H * W * Cout;
+    const long long nw = (long long)Cout * Cin * R * S;
     if (Cin > 1 && !aligned16(x)) return SC_ERR_ALIGN;
     if (Cout > 1 && !aligned16(y)) return SC_ERR_ALIGN;
     const size_t ybytes = (size_t)ny * sizeof(float);
@@ -231,6 +240,55 @@ int conv2d_fwd(const float *x, const float *w, const float *b, float *y, int N, 
     }
     if (rc == SC_OK && need_out) {
         e = sc::launch_transpose_batched(y_nhwc, y, N, (long long)H * W, Cout, st);
+        if (e != cudaSuccess) rc = cuda_fail(e);
+    }
+    cudaError_t ef = sc::workspace_free(ws, st);
+    if (rc == SC_OK && ef != cudaSuccess) rc = cuda_fail(ef);
+    return rc;
+}
+
+int conv2d_chain_fwd_host(const float *x_host, float *y_host, int N, int H, int W, int Cin, int n_layers,
+                          const sc_conv_layer *layers, sc_stream_t stream)
+{
+    if (!x_host || !y_host || !layers) return SC_ERR_NULL;
+    if (n_layers < 1 || n_layers > SC_CHAIN_MAX_LAYERS) return SC_ERR_SHAPE;
+    // every layer's shape first: nothing is enqueued for a chain that fails
+    int cin = Cin, cmax = 1;
+    for (int l = 0; l < n_layers; ++l) {
+        const sc_conv_layer &L = layers[l];
+        if (!L.w) return SC_ERR_NULL;
+        const int rc = sc::check_conv_shape(N, H, W, cin, L.Cout, L.R, L.S, SC_NHWC, L.act);
+        if (rc != SC_OK) return rc;
+        if (L.Cout > cmax) cmax = L.Cout;
+        cin = L.Cout;
+    }
+    const long long px = (long long)N * H * W;
+    const size_t in_bytes = (size_t)(px * Cin) * sizeof(float);
+    const size_t out_bytes = (size_t)(px * cin) * sizeof(float);
+    const size_t act_bytes = (((size_t)(px * cmax) * sizeof(float)) + 255) & ~(size_t)255;
+    const size_t off = (in_bytes + 255) & ~(size_t)255;
+    // [input][activation A][activation B]: layer l reads the input (l = 0)
+    // or buffer (l - 1) % 2 and writes buffer l % 2
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    void *ws = nullptr;
+    cudaError_t e = sc::workspace_alloc(&ws, off + (n_layers > 1 ? 2 : 1) * act_bytes, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    char *base = static_cast<char *>(ws);
+    float *act_buf[2] = {reinterpret_cast<float *>(base + off), reinterpret_cast<float *>(base + off + act_bytes)};
+    int rc = SC_OK;
+    e = cudaMemcpyAsync(base, x_host, in_bytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) rc = cuda_fail(e);
+    const float *in = reinterpret_cast<const float *>(base);
+    cin = Cin;
+    for (int l = 0; l < n_layers && rc == SC_OK; ++l) {
+        const sc_conv_layer &L = layers[l];
+        const sc::ConvArgs a{in, L.w, L.b, act_buf[l & 1], N, H, W, cin, L.Cout, L.R, L.S, L.act};
+        rc = conv_nhwc_status(a, st);
+        in = act_buf[l & 1];
+        cin = L.Cout;
+    }
+    if (rc == SC_OK) {
+        e = cudaMemcpyAsync(y_host, in, out_bytes, cudaMemcpyDeviceToHost, st);
         if (e != cudaSuccess) rc = cuda_fail(e);
     }
     cudaError_t ef = sc::workspace_free(ws, st);

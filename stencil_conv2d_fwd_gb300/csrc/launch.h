@@ -148,6 +148,9 @@ cudaError_t workspace_free(void *p, cudaStream_t st);
 // its contract: SC_OK when the call may launch, else the status to return.
 int check_conv_args(const float *x, const float *w, const float *b, const float *y, int N, int H, int W, int Cin,
                     int Cout, int R, int S, int layout, int act);
+// The part of those checks that needs no pointers: sizes, filter size,
+// layout, activation and the supported channel counts.
+int check_conv_shape(int N, int H, int W, int Cin, int Cout, int R, int S, int layout, int act);
 // Records e for sc_last_cuda_error (per host thread) and returns SC_ERR_CUDA.
 int record_cuda_error(cudaError_t e);
 

@@ -131,3 +131,28 @@ def test_conv_wait_expiry_hook_argument_errors():
     assert sc.sc_test_conv_wait_expiry(A16, A16, None, B16, 1, 4, 4, 6, 4, 0, 10, stream=0) == sc.SC_ERR_UNSUPPORTED
     assert sc.sc_test_conv_wait_expiry(A16 + 4, A16, None, B16, 1, 4, 4, 4, 4, 0, 10, stream=0) == sc.SC_ERR_ALIGN
     assert sc.sc_test_conv_wait_expiry(A16, A16, None, A16, 1, 4, 4, 4, 4, 0, 10, stream=0) == sc.SC_ERR_ALIAS
+
+
+NET = [(1 << 28, None, 8, 5, 5, 1), (1 << 28, None, 8, 3, 3, 1), (1 << 28, None, 4, 3, 3, 0)]
+
+
+@pytest.mark.parametrize("change,expect", [
+    (dict(x=None), sc.SC_ERR_NULL),
+    (dict(y=None), sc.SC_ERR_NULL),
+    (dict(layers=[]), sc.SC_ERR_SHAPE),
+    (dict(layers=NET * 22), sc.SC_ERR_SHAPE),                      # more than SC_CHAIN_MAX_LAYERS
+    (dict(N=0), sc.SC_ERR_SHAPE),
+    (dict(layers=[(None, None, 8, 5, 5, 1)] + NET[1:]), sc.SC_ERR_NULL),
+    (dict(layers=[NET[0], (1 << 28, None, 8, 2, 3, 1)]), sc.SC_ERR_UNSUPPORTED),
+    (dict(layers=[NET[0], (1 << 28, None, 6, 3, 3, 1)]), sc.SC_ERR_UNSUPPORTED),
+    (dict(layers=[(1 << 28, None, 6, 3, 3, 1)]), sc.SC_ERR_UNSUPPORTED),   # Cin 1 -> Cout 6
+    (dict(layers=NET[:2] + [(1 << 28, None, 4, 3, 3, 2)]), sc.SC_ERR_UNSUPPORTED),
+    (dict(Cin=6, layers=NET[1:]), sc.SC_ERR_UNSUPPORTED),
+])
+def test_chain_argument_errors(change, expect):
+    """conv2d_chain_fwd_host checks every layer (its Cin the previous Cout) by
+    conv2d_fwd's rules before it enqueues anything (host-side only)."""
+    a = dict(x=A16, y=B16, N=1, H=8, W=8, Cin=1, layers=NET)
+    a.update(change)
+    rc = sc.conv2d_chain_fwd_host(a["x"], a["y"], a["N"], a["H"], a["W"], a["Cin"], a["layers"], stream=0)
+    assert rc == expect, sc.sc_status_string(rc)
