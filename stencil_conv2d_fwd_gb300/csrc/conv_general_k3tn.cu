@@ -24,13 +24,13 @@ static const TuneCand k3_n16[] = {
     {"TMA F16 W3 2x48", k3_tma_f16_w3_h2},
     {"TMA F8 W3 4x96", k3_tma_f8_w3_h4},
     {"TMA F8 W3 2x96", k3_tma_f8_w3_h2},
-    {"small image 4x32", launch_conv_small},
+    {"small image 2x64", launch_conv_small},
 };
 static const TuneCand k3_n8[] = {
     {"heuristic", launch_conv_general_k3},
     {"F8 W8 4x256", cand_n<8, 8, 4, 256, 2>},
     {"TMA F8 W5 4x160", k3_tma_f8_w5_h4},
-    {"small image 4x32", launch_conv_small},
+    {"small image 2x64", launch_conv_small},
 };
 static const TuneCand k3_n4[] = {
     {"heuristic", launch_conv_general_k3},
@@ -46,7 +46,7 @@ static const TuneCand k3_n4[] = {
     {"TMA F4 W5 8x160 4 stages", k3_tma_f4_w5_h8_s4},
     {"N4 W5 8x160 4 stages", k3_n4_h8_s4},
     {"N4 W5 8x160 c16", k3_n4_h8_c16},
-    {"small image 4x32", launch_conv_small},
+    {"small image 2x64", launch_conv_small},
 };
 
 const TuneCand *k3_narrow_table(const ConvArgs &a, int *n)
