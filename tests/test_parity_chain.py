@@ -6,7 +6,7 @@ equal, bit for bit, the same layers run one conv2d_fwd call at a time on
 device buffers; each of those layers is held to the fp64 oracle fed the
 GPU's own input to it, at the fp32 bound 1e-5 * A.  Covered: the 3-layer
 net of workload 3 at a reduced and at its full size, pinned and pageable
-host buffers, a chain of one layer, and a batch of images.
+host buffers, chains of one layer, and batches of images.
 """
 import numpy as np
 import pytest
@@ -102,3 +102,14 @@ def test_chain_of_mixed_filters(oracle_mod, cuda_dev, sc):
     keep, spec = _layers_on_device(rng_layers, cuda_dev)
     ref = _chain_layer_by_layer(oracle_mod, x, rng_layers, spec, cuda_dev)
     assert np.array_equal(_chain_host(x, spec, cuda_dev), ref)
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+def test_chain_of_one_single_channel_layer(oracle_mod, cuda_dev, sc, pinned):
+    """A chain of one layer with one input channel (the tiled single-channel
+    kernel, whose stores go through shared memory and the TMA), pinned and
+    pageable host buffers."""
+    c = S.conv_case(1320, 2, 1, 32, 29, 140, 5, 5, act=1)
+    keep, spec = _layers_on_device(c.layers, cuda_dev)
+    ref = _chain_layer_by_layer(oracle_mod, c.x, c.layers, spec, cuda_dev)
+    assert np.array_equal(_chain_host(c.x, spec, cuda_dev, pinned=pinned), ref)
