@@ -716,6 +716,9 @@ def per_config(sc, S, dev, stream, flush, fp32_tflops, hbm_gbs, hbm_src):
                      "roofline_frac": round(max(t_c, t_m) / (med * 1e-3), 4),
                      "tolerance": "5e-3 * sum|x*w| + 2^-8 |y| (bf16 operands and storage)",
                      "bf16_peak_tflops": round(bf16_tflops, 1)}
+        kern = time_in_graph(call_bf, flush, stream)
+        out[name].update({"ms_kernel": round(kern, 5),
+                          "roofline_frac_kernel": round(max(t_c, t_m) / (kern * 1e-3), 4)})
 
     # layer fusion (f2): layers 2 and 3 of the net in one tensor-core pass,
     # the 32-channel intermediate kept on chip (TF32 operands)
