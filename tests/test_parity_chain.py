@@ -113,3 +113,34 @@ def test_chain_of_one_single_channel_layer(oracle_mod, cuda_dev, sc, pinned):
     keep, spec = _layers_on_device(c.layers, cuda_dev)
     ref = _chain_layer_by_layer(oracle_mod, c.x, c.layers, spec, cuda_dev)
     assert np.array_equal(_chain_host(c.x, spec, cuda_dev, pinned=pinned), ref)
+
+
+def test_chain_captured_in_a_cuda_graph(oracle_mod, cuda_dev, sc):
+    """The call is stream-ordered throughout (pool buffers, copies, launches),
+    so it can be captured into a CUDA graph; two replays on new host data
+    give the results of direct calls."""
+    c = S.config(3, scale={"h": 37, "w": 161})
+    keep, spec = _layers_on_device(c.layers, cuda_dev)
+    N, Cin, H, W = c.x.shape
+    cout = spec[-1][2]
+    x_host = torch.from_numpy(nchw_to_nhwc(c.x)).pin_memory()
+    y_host = torch.full((N * H * W * cout,), np.nan, dtype=torch.float32).pin_memory()
+    ref = _chain_host(c.x, spec, cuda_dev, pinned=True)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            rc = sc.conv2d_chain_fwd_host(x_host, y_host, N, H, W, Cin, spec, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    assert rc == sc.SC_OK, sc.sc_status_string(rc)
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(nhwc_to_nchw(y_host.numpy().reshape(N, H, W, cout)), ref)
+    # new input in the same pinned buffer: the replay reads it
+    x2 = (c.x * 0.5).astype(np.float32)
+    x_host.copy_(torch.from_numpy(nchw_to_nhwc(x2)))
+    y_host.fill_(np.nan)
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(nhwc_to_nchw(y_host.numpy().reshape(N, H, W, cout)), _chain_host(x2, spec, cuda_dev))
