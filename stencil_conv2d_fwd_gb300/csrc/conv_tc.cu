@@ -757,7 +757,7 @@ static cudaError_t launch_tc_cg(const ConvArgs &a, cudaStream_t st)
     PFN_cuTensorMapEncodeTiled_v12000 encode = tc_tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
     // NHWC activations as a 4-D tensor (C, W, H, N); box = the channels of
-    // one sub-buffer (32 fp32 or 16 bf16: one swizzled row per pixel;
+    // one sub-buffer (32 fp32 or 32 bf16: one swizzled row per pixel;
     // channels past Cin read as zero) x 32 padded columns x THh (= TR + 2)
     // rows of one image
     CUtensorMap tm;
@@ -768,7 +768,8 @@ static cudaError_t launch_tc_cg(const ConvArgs &a, cudaStream_t st)
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     if (encode(&tm, OP::ESZ == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                const_cast<float *>(a.x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               OP::ROWB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_32B,
+               OP::ROWB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                               : (OP::ROWB == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B),
                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorNotSupported;
     // NHWC output as (C, W, H, N); box = the group's CG channels x TC pixels

@@ -21,17 +21,18 @@ constexpr int CH = 32;          // channels per stage (one swizzled row per pixe
 // Operand kinds.  Either way a K step (one MMA's K) is 32 bytes of a pixel's
 // channels and one 16-byte chunk of a B row holds CU = KC / 2 channels.  A
 // 32-channel stage is SUB sub-buffers, each filled by one TMA box, with one
-// ROWB-byte swizzled row per padded pixel.  The row widths are chosen so that
-// the tensor core's read of a 32-byte K slice of 8 consecutive rows touches
-// every 16-byte bank group exactly twice (no conflicts): 128-byte rows with
-// 128-byte swizzling, or 32-byte rows with 32-byte swizzling (64-byte rows
-// with 64-byte swizzling would put rows r and r + 2 on the same banks).
+// ROWB-byte swizzled row per padded pixel.  With the row width equal to the
+// swizzle span (128-byte rows with 128-byte swizzling, 64-byte rows with
+// 64-byte swizzling), the tensor core's read of a 32-byte K slice of 8
+// consecutive rows touches every 16-byte bank group exactly twice (no
+// conflicts; tests/test_kernel_swizzle.py checks each layout).
 //  * OpTF32: fp32 activations, TF32 MMA (kind::tf32), K step = 8 channels;
 //    one 128-byte row of 32 channels per pixel (4 K steps per row).
 //  * OpBF16: bf16 activations, BF16 MMA (kind::f16), K step = 16 channels;
-//    two sub-buffers of 32-byte rows (16 channels, one K step each).  The
-//    fp32 filters are rounded to bf16 (to nearest even) when the CTA stages
-//    them.
+//    one 64-byte row of 32 channels per pixel (2 K steps per row; two
+//    32-byte-row sub-buffers, one TMA box each, took 37.1 against 36.1 us on
+//    the 32 -> 32 layer, with the same results).  The fp32 filters are
+//    rounded to bf16 (to nearest even) when the CTA stages them.
 //  * OpTF32x3: OpTF32's layout with every operand split into a TF32 head and
 //    a remainder, v = hi(v) + lo(v), hi(v) = v with its 13 low mantissa bits
 //    cleared (exactly a TF32 value), lo(v) = v - hi(v) (exact in fp32, at most
@@ -56,8 +57,8 @@ struct OpTF32 {
     static constexpr bool X3 = false;
 };
 struct OpBF16 {
-    static constexpr int ESZ = 2, KC = 16, ROWB = 32, SUB = 2;
-    static constexpr uint32_t A_LAYOUT = 6, FMT = 1;   // descriptor layout 32B swizzle; BF16
+    static constexpr int ESZ = 2, KC = 16, ROWB = 64, SUB = 1;
+    static constexpr uint32_t A_LAYOUT = 4, FMT = 1;   // descriptor layout 64B swizzle; BF16
     static constexpr bool X3 = false;
 };
 struct OpTF32x3 {

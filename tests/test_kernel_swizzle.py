@@ -403,3 +403,22 @@ def test_small_filter_and_partial_sum_accesses():
                 continue
             banks = [((e % KK) * 20 + e // KK) % 32 for e in es]
             assert max(banks.count(bk) for bk in set(banks)) <= 4
+
+
+# ---------------------------------------------------------------------------
+# conv_tc.cu: the tensor core reads a K step of A as a 32-byte slice of 8
+# consecutive padded-pixel rows.  With the row width equal to the TMA swizzle
+# span (TF32: 128-byte rows, 128-byte swizzle; BF16: 64-byte rows, 64-byte
+# swizzle), the 16 chunks of a slice fall on every 16-byte bank group exactly
+# twice, for every K step and any 8-row-aligned start.
+
+@pytest.mark.parametrize("rowb", [128, 64, 32])
+def test_tensor_core_k_slices_spread_over_all_bank_groups(rowb):
+    for k in range(rowb // 32):                 # K steps within a row
+        for r0 in range(0, 64, 8):
+            groups = []
+            for r in range(r0, r0 + 8):
+                for c in range(2):
+                    byte = tma_swizzled_byte(r * rowb + 32 * k + 16 * c, rowb)
+                    groups.append((byte // 16) % 8)
+            assert sorted(groups) == sorted(list(range(8)) * 2), (rowb, k, r0)
