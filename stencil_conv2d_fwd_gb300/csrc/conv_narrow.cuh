@@ -16,8 +16,17 @@
 //    registers, so the next step starts on data in hand.  The steps of a
 //    tile are unrolled (NK = Cin / C_SH of them), so the prefetched rows
 //    need no register moves.
-//  * The producer issues the first NSTAGE copies before the CTA stages its
-//    filters, so the filter loads and the first activation copies overlap.
+//  * The producer issues the first copy before the CTA stages its filters,
+//    so the filter loads and the first activation copies overlap, and the
+//    rest of the ring's first fill once that copy has landed: at the start
+//    of a launch every CTA's copies arrive together, and a CTA whose whole
+//    ring is in flight waits for most of it before its first stage is
+//    complete (per-CTA timestamps on 1280 x 720: the first stage landed
+//    6.1 us into the launch, then a tile every 7.7 us).
+//  * The tensor map promotes L2 fills to 64 bytes, not 128: a step's copy
+//    takes 32 bytes (8 channels) of each 128-byte pixel, and 128-byte
+//    promotion made the first step of a tile fetch all 32 channels at once
+//    (49.4 -> 48.2 us with the staggered fill, 46.8 us with both).
 // The copy protocol (one 4-D TMA box per step into a ring of NSTAGE
 // swizzled stages, full/empty mbarriers, bounded waits that record
 // SC_ERR_DEVICE_TIMEOUT) and the shared-memory layout are conv_tma.cuh's
@@ -96,13 +105,14 @@ __global__ void __launch_bounds__(C::NT, C::MINB)
         tma_load_4d(stage0 + slot * C::STAGE_BYTES, &tm, (i % C::NK) * C::C_SH, x0 - 1, y0 - 1, n, full(slot));
     };
     const int pre = total < C::NSTAGE ? total : C::NSTAGE;
+    const int pre0 = pre < 1 ? pre : 1;   // issued before the filters
     if (warp == C::TH && lane == 0) {
         for (int i = 0; i < C::NSTAGE; ++i) {
             mbar_init(full(i), 1);
             mbar_init(empty(i), C::TH);
         }
         fence_mbar_init();
-        for (int i = 0; i < pre; ++i) issue(i);   // before the filters: the two loads overlap
+        for (int i = 0; i < pre0; ++i) issue(i);
     }
     // filters as float4 units [ci][r][s] of 4 output channels, zero where
     // the R x S filter has no tap or co >= Cout
@@ -123,6 +133,10 @@ __global__ void __launch_bounds__(C::NT, C::MINB)
         // the consumers have released
         if (lane != 0) return;
         bool failed = false;
+        if (pre > pre0) {   // the ring's first fill, once the first copy has landed
+            (void)mbar_wait_bounded_idle(full(0), 0, timeout_ns, 64);
+            for (int k = pre0; k < pre; ++k) issue(k);
+        }
         int i = pre;
         for (; i < total; ++i) {
             const int slot = i % C::NSTAGE;
@@ -294,7 +308,7 @@ cudaError_t launch_conv_n4(const ConvArgs &a, cudaStream_t st, unsigned long lon
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     const CUtensorMapSwizzle swz = C::PXB == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B;
     if (encode(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(a.x), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_64B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorNotSupported;
     const size_t smem = C::smem_bytes();

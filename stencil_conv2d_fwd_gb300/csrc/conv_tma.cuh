@@ -213,15 +213,16 @@ __global__ void __launch_bounds__(C::NT, C::MINB)
     };
     const int my_tiles = (int)blockIdx.x < ntiles ? (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int pre = my_tiles * nk < C::NSTAGE ? my_tiles * nk : C::NSTAGE;
+    const int pre0 = pre < 1 ? pre : 1;   // issued before the filters
     if (warp == C::NC && lane == 0) {
         for (int i = 0; i < C::NSTAGE; ++i) {
             mbar_init(full(i), 1);
             mbar_init(empty(i), C::NC);
         }
         fence_mbar_init();
-        // the first copies go out before the filters are staged, so the two
+        // the first copy goes out before the filters are staged, so the two
         // loads overlap
-        for (int i = 0; i < pre; ++i) issue(i, blockIdx.x + (i / nk) * gridDim.x, i % nk);
+        for (int i = 0; i < pre0; ++i) issue(i, blockIdx.x + (i / nk) * gridDim.x, i % nk);
     }
     // large banks (64 -> 64: 147 KB a CTA, 146.7 -> 128.4 us) from 16-byte
     // loads; small ones (16 -> 16: 9 KB) keep the asynchronous copies, which
@@ -244,6 +245,10 @@ __global__ void __launch_bounds__(C::NT, C::MINB)
         if (lane != 0) return;
         int issued = 0;
         bool failed = false;
+        if (pre > pre0) {   // the ring's first fill, once the first copy has landed
+            (void)mbar_wait_bounded_idle(full(0), 0, timeout_ns, 64);
+            for (int i = pre0; i < pre; ++i) issue(i, blockIdx.x + (i / nk) * gridDim.x, i % nk);
+        }
         for (int t = blockIdx.x; t < ntiles && !failed; t += gridDim.x) {
             for (int k = 0; k < nk; ++k, ++issued) {
                 if (issued < pre) continue;   // issued before the filters
@@ -489,8 +494,11 @@ cudaError_t launch_conv_tma(const ConvArgs &a, cudaStream_t st, int drop_copy = 
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     const CUtensorMapSwizzle swz = C::PXB == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
                                    : C::PXB == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+    // L2 fills promoted to 64 bytes: a step copies C_SH channels (32 or 64
+    // bytes) of each pixel, and 128-byte promotion fetched the other steps'
+    // channels with the first step (32 -> 32: 276.3 -> 275.0 us)
     if (encode(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(a.x), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_64B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorNotSupported;
     const size_t smem = C::smem_bytes(cin_pad);
